@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the KV-cache attention hot path on one GB300 (or N replicas).
+
+A step is one whole run of the multi-user streaming workload: reset, then for each
+of its chunks reserve the slots (advance), write the chunk's K/V at the device-held
+slots (write) and attend the chunk's queries over the sink+window ring (attend).
+Default workload: 8 users sharing one chunk timeline, bf16, H = 40, D = 128, chunk
+4680 tokens, sink 4680, window 32760, 8 chunks (125.6 TFLOP per step).  The K/V
+stores (5.4 GB) are far larger than L2, so no flush is needed between steps.
+
+Prints one JSON line.  ``value`` is chunk-attention TFLOP/s over the whole step
+(write and advance time included); the line also carries the write and decode
+bandwidth, the roofline of the dominant kernel, the end-to-end figure through the
+binding with host buffers, and the CPU oracle timed on a bounded sample.
+
+``--impl reference`` times the CPU fp64 oracle as the reference arm instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from diffusion_serving_gb300 import workloads as wl  # noqa: E402
+
+WORKLOADS = {w.name: w for w in wl.ALL if w.layout == "circular"}
+DEFAULT = wl.MULTI_USER.name
+METRIC = "chunk-attention TFLOP/s + decode/write HBM GB/s on 1 GB300, as % of roofline"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sust=d["bf16_tflops_sustained"], src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sust=1700.0, src="fallback")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_init(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+        return rank, world, dist
+    if torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return 0, 1, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x, dist):
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.dev = device_index
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def ring_flops(w):
+    """Algorithmic flops of one step (every chunk, every rewrite, valid slots only)."""
+    total = 0.0
+    per_attend = []
+    for c in range(w.n_chunks):
+        kv = min((c + 1) * w.chunk, w.window)
+        f = wl.attention_flops(w.chunk, kv, w.heads, w.head_dim) * w.batch
+        for _ in range(w.rewrites):
+            per_attend.append(f)
+            total += f
+    return total, per_attend
+
+
+def make_inputs(w, device, pool):
+    """Distinct (q, k, v) per chunk (and rewrite, up to ``pool`` sets), resident on device."""
+    sets = []
+    for c in range(w.n_chunks):
+        for r in range(w.rewrites):
+            if len(sets) < pool:
+                sets.append(wl.chunk_inputs(w, c, r, device=device))
+    return sets
+
+
+def run_step(cache, w, inputs, out, stream, ev=None, kvc=None):
+    """One step; when ``ev`` is given, record events around each write and attend."""
+    launches = 0
+    cache.reset(stream=stream)
+    launches += 1
+    i = 0
+    for c in range(w.n_chunks):
+        cache.advance(stream=stream)
+        launches += 1
+        for r in range(w.rewrites):
+            q, k, v = inputs[i % len(inputs)]
+            i += 1
+            if ev is not None:
+                ev["w"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                ev["w"][-1][0].record(stream)
+            cache.write(k, v, stream=stream)
+            if ev is not None:
+                ev["w"][-1][1].record(stream)
+                ev["a"].append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+                ev["a"][-1][0].record(stream)
+            cache.attend(q, out, stream=stream)
+            if ev is not None:
+                ev["a"][-1][1].record(stream)
+            launches += 2
+    return launches
+
+
+def decode_bench(kvc, peaks, reps=50):
+    """Split-KV decode on the active-prefix workload shape: latency of a mean-length
+    step and bandwidth at a full 32768-slot prefix."""
+    w = wl.DECODE
+    cache = kvc.KVCache(w.batch, w.heads, w.kv_heads, w.head_dim, torch.float16, "linear", capacity=w.capacity)
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    cache.k_store.normal_(generator=g)
+    cache.v_store.normal_(generator=g)
+    q = torch.randn(1, 1, w.heads, w.head_dim, device="cuda", generator=g).half()
+    out = torch.empty_like(q)
+    row = w.kv_heads * w.head_dim * 2
+    res = {}
+    s = torch.cuda.current_stream()
+    flush = torch.empty(wl.l2_flush_bytes(), dtype=torch.uint8, device="cuda")
+    for name, n in (("mean_step_kv490", wl.DECODE_PROMPT + wl.DECODE_STEPS // 2), ("full_prefix_kv32768", w.capacity)):
+        cache.set_lengths(kv_len=torch.tensor([n], dtype=torch.int32, device="cuda"))
+        for _ in range(3):
+            cache.attend(q, out)
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            cache.attend(q, out)
+            b.record(s)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e-3)
+        t = float(np.median(times))
+        nbytes = 2 * n * row
+        res[name] = {"kv_len": n, "us": t * 1e6, "GB/s": nbytes / t / 1e9, "frac": nbytes / t / 1e9 / peaks["hbm"],
+                     "bytes": nbytes}
+    assert cache.get_error() == 0
+    return res
+
+
+def cpu_oracle_sample(w, budget_s=12.0):
+    """Time the fp64 oracle on sampled query rows of a full-window attend."""
+    from oracle import kvc_oracle as orc
+    kv = w.window
+    rng = np.random.default_rng(0)
+    k = rng.standard_normal((kv, 1, w.head_dim)).astype(np.float64)
+    v = rng.standard_normal((kv, 1, w.head_dim)).astype(np.float64)
+    rows = 64
+    flops = 0.0
+    t0 = time.perf_counter()
+    calls = 0
+    while time.perf_counter() - t0 < budget_s:
+        q = rng.standard_normal((rows, 1, w.head_dim))
+        orc.attend(q, k, v)
+        flops += wl.attention_flops(rows, kv, 1, w.head_dim)
+        calls += 1
+    dt = time.perf_counter() - t0
+    return flops / dt / 1e12, dt, calls * rows
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        return max((i.get("num_threads", 1) for i in info), default=1)
+    except Exception:
+        return host_cores()
+
+
+def ours(args):
+    rank, world, dist = dist_init(args.gpus)
+    from diffusion_serving_gb300 import kvc
+    w = WORKLOADS[args.workload]
+    peaks = load_peaks()
+    dtype = wl.DTYPES[w.dtype]
+    stream = torch.cuda.current_stream()
+    cache = kvc.KVCache(w.batch, w.heads, w.kv_heads, w.head_dim, dtype, w.layout, sink=w.sink, window=w.window,
+                        chunk=w.chunk)
+    inputs = make_inputs(w, "cuda", pool=w.n_chunks * w.rewrites)
+    out = torch.empty_like(inputs[0][0])
+    step_flops, per_attend = ring_flops(w)
+
+    for _ in range(args.warmup):
+        run_step(cache, w, inputs, out, stream)
+    torch.cuda.synchronize()
+    assert cache.get_error() == 0
+
+    ev = {"w": [], "a": []}
+    launches = 0
+    with Clocks(torch.cuda.current_device()) as clk:
+        barrier(dist)
+        torch.cuda.synchronize()
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(args.steps):
+            launches += run_step(cache, w, inputs, out, stream, ev)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+    elapsed = start.elapsed_time(stop) * 1e-3
+    elapsed = max_over_ranks(elapsed, dist)
+    err = cache.get_error()
+    assert err == 0, f"device error bits {err:#x}"
+
+    attend_t = [a.elapsed_time(b) * 1e-3 for a, b in ev["a"]]
+    write_t = [a.elapsed_time(b) * 1e-3 for a, b in ev["w"]]
+    attend_flops = per_attend * args.steps
+    avg_attend_flops = float(np.mean(attend_flops))
+    avg_attend_t = float(np.mean(attend_t))
+    achieved = avg_attend_flops / avg_attend_t / 1e12
+    row_bytes = w.kv_heads * w.head_dim * 2
+    write_bytes = 2 * 2 * w.batch * w.chunk * row_bytes      # K and V, read + write
+    write_gbs = write_bytes / float(np.mean(write_t)) / 1e9
+
+    value = world * step_flops * args.steps / elapsed / 1e12
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(elapsed / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "kv_heads": w.kv_heads,
+                   "head_dim": w.head_dim, "chunk": w.chunk, "sink": w.sink, "window": w.window,
+                   "chunks_per_step": w.n_chunks, "rewrites": w.rewrites, "tflop_per_step": step_flops / 1e12,
+                   "l2": "inputs larger than L2 (K/V stores %.1f GB)" % (2 * cache.k_store.numel() * 2 / 1e9),
+                   "parallelism": f"replicas x{world}"},
+        "gpu_launches": launches,
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_sust"],
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_sust"], 4), "traffic": None,
+                     "kernel": "chunk attention (attend)", "peak_kind": f"bf16 dense sustained, {peaks['src']}",
+                     "attend_ms_avg": round(avg_attend_t * 1e3, 3)},
+        "write": {"GB/s": round(write_gbs, 1), "frac": round(write_gbs / peaks["hbm"], 4),
+                  "bytes_per_launch": write_bytes, "us_avg": round(float(np.mean(write_t)) * 1e6, 2)},
+    }
+    clocks = clk.summary()
+    if clocks is not None:
+        result["clocks"] = clocks
+    result["decode"] = decode_bench(kvc, peaks)
+
+    # end to end through the binding: host (pinned) inputs copied in, output read back
+    if True:
+        host = [tuple(t.cpu().pin_memory() for t in s) for s in inputs]
+        dev = [tuple(torch.empty_like(t) for t in inputs[0]) for _ in range(2)]
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host[0]) * w.n_chunks * w.rewrites
+        d2h = out_host.numel() * out_host.element_size() * w.n_chunks * w.rewrites
+
+        def e2e_step():
+            cache.reset()
+            i = 0
+            for c in range(w.n_chunks):
+                cache.advance()
+                for r in range(w.rewrites):
+                    q, k, v = dev[i % 2]
+                    hq, hk, hv = host[i % len(host)]
+                    q.copy_(hq, non_blocking=True)
+                    k.copy_(hk, non_blocking=True)
+                    v.copy_(hv, non_blocking=True)
+                    cache.write(k, v)
+                    cache.attend(q, out)
+                    out_host.copy_(out, non_blocking=True)
+                    i += 1
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(dist)
+        t0 = time.perf_counter()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        barrier(dist)
+        e2e_t = max_over_ranks(a.elapsed_time(b) * 1e-3, dist)
+        result["e2e"] = {"value": round(world * step_flops * args.steps / e2e_t / 1e12, 2), "unit": "TFLOP/s",
+                         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                         "ms_per_step": round(e2e_t / args.steps * 1e3, 3)}
+    if rank == 0:
+        tf, dt, nrows = cpu_oracle_sample(w)
+        result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                                  "sample": f"{nrows} query rows x {w.window} keys x 1 head (D={w.head_dim}) of a "
+                                            f"full-window attend, fp64 NumPy, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU fp64 oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+def reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, budget_s=1.0)
+    t_total, flops_total, rows_total = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        tf, dt, nrows = cpu_oracle_sample(w, budget_s=5.0)
+        t_total += dt
+        flops_total += tf * 1e12 * dt
+        rows_total += nrows
+    value = flops_total / t_total / 1e12
+    cores = blas_threads()
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_total} query rows x {w.window} keys x 1 head per run, fp64 NumPy"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference(args)
+    else:
+        ours(args)
+
+
+if __name__ == "__main__":
+    main()

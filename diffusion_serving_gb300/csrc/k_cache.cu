@@ -1,0 +1,176 @@
+// Cache bookkeeping and slot writes.
+//
+//  * k_advance   slot reservation for the next chunk (flashdreams issue "add an opt-in
+//                circular KV policy for streaming attention", "proposed boundary":
+//                reservation is separate from writes and lives in device memory).
+//  * k_reset     row lifecycle reset (same section).
+//  * k_set_lengths  active prefix kv_len (fish-speech PR "pass only active KV cache
+//                prefix to SDPA", "Change") and packed offsets cu_seqlens (TensorRT-LLM
+//                PR "FA4 variable-length cross-attention", Description).
+//  * k_write     index_copy-style row scatter (lingbot-world PR "refactor(kv):
+//                index_copy_ for KV-cache writes", Summary): bytes copied unchanged in
+//                16-byte vectors, slot taken from device memory so replays of a
+//                captured graph write the slot the device holds.
+#include "kvc_internal.h"
+
+namespace {
+
+__global__ void k_advance(int32_t* __restrict__ meta, int B, int row, int n, int layout, int sink,
+                          int window, int chunk, int cap) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    if (row >= 0 && b != row) continue;
+    int32_t* r = meta + kvc_meta_row(b);
+    const int k = r[KVC_ROW_CHUNKS];
+    if (layout == KVC_CIRCULAR) {
+      const int64_t first = (int64_t)k * chunk;
+      int base;
+      if (first < window) {
+        base = (int)first;                               // still filling
+      } else {
+        const int roll = (window - sink) / chunk;        // rolling chunks
+        const int64_t idx = ((int64_t)k - sink / chunk) % roll;
+        base = sink + (int)idx * chunk;                  // oldest rolling chunk
+      }
+      const int64_t filled = first + chunk < window ? first + chunk : window;
+      r[KVC_ROW_CHUNKS] = k + 1;
+      r[KVC_ROW_BASE] = base;
+      r[KVC_ROW_FILLED] = (int)filled;
+      r[KVC_ROW_KVLEN] = (int)filled;
+    } else {  // LINEAR
+      const int filled = r[KVC_ROW_FILLED];
+      if ((int64_t)filled + n > cap) {
+        atomicOr(meta + KVC_META_ERR, KVC_DEV_OVERFLOW);
+        continue;
+      }
+      r[KVC_ROW_CHUNKS] = k + 1;
+      r[KVC_ROW_BASE] = filled;
+      r[KVC_ROW_FILLED] = filled + n;
+      r[KVC_ROW_KVLEN] = filled + n;
+    }
+  }
+}
+
+__global__ void k_reset(int32_t* __restrict__ meta, int B, int row) {
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    if (row >= 0 && b != row) continue;
+    int32_t* r = meta + kvc_meta_row(b);
+    r[KVC_ROW_CHUNKS] = 0;
+    r[KVC_ROW_BASE] = 0;
+    r[KVC_ROW_FILLED] = 0;
+    r[KVC_ROW_KVLEN] = 0;
+  }
+}
+
+__global__ void k_set_lengths(int32_t* __restrict__ meta, int B, int cap, const int32_t* __restrict__ kv_len,
+                              const int32_t* __restrict__ cu) {
+  __shared__ int ok;
+  if (kv_len != nullptr) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      const int n = kv_len[b];
+      if (n < 1 || n > cap) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_KVLEN);
+      else meta[kvc_meta_row(b) + KVC_ROW_KVLEN] = n;
+    }
+  }
+  if (cu == nullptr) return;
+  if (threadIdx.x == 0) {
+    int good = cu[0] == 0;
+    for (int b = 0; b < B && good; ++b) good = cu[b + 1] > cu[b];
+    good = good && cu[B] <= cap;
+    ok = good;
+    if (!good) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_CUSEQ);
+  }
+  __syncthreads();
+  if (!ok) return;
+  for (int b = threadIdx.x; b <= B; b += blockDim.x) meta[kvc_meta_cu(B) + b] = cu[b];
+  for (int b = threadIdx.x; b < B; b += blockDim.x) meta[kvc_meta_row(b) + KVC_ROW_KVLEN] = cu[b + 1] - cu[b];
+}
+
+// One warp per (tensor, row b, token i): the warp resolves the destination row once,
+// then its lanes copy the row's 16-byte vectors, 4 loads in flight per lane before
+// the stores.  Destination row of (b, i):
+//   slots given:  b * cap + slots[i]
+//   reserved:     b * cap + base_b + i      (LINEAR also requires base_b + i < filled_b)
+//   packed:       cu[b] + i for i < len_b (later tokens are padding and are skipped)
+constexpr int kWriteThreads = 256;
+constexpr int kWriteUnroll = 4;
+
+__global__ void __launch_bounds__(kWriteThreads)
+k_write(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* __restrict__ kdst,
+        uint4* __restrict__ vdst, int32_t* __restrict__ meta, const int32_t* __restrict__ slots, int B, int n,
+        int row_vecs, int cap, int layout) {
+  const int lane = threadIdx.x & 31;
+  const int rows_per_tensor = B * n;
+  const int rows = 2 * rows_per_tensor;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+    const int t = r >= rows_per_tensor;
+    const int e = r - (t ? rows_per_tensor : 0);
+    const int b = e / n;
+    const int i = e - b * n;
+    int64_t drow = -1;
+    if (layout == KVC_PACKED) {
+      const int32_t* cu = meta + kvc_meta_cu(B);
+      const int lo = cu[b], hi = cu[b + 1];
+      if (i < hi - lo && lo >= 0 && hi <= cap) drow = lo + i;
+    } else if (slots != nullptr) {
+      const int s = slots[i];
+      if (s >= 0 && s < cap) drow = (int64_t)b * cap + s;
+      else if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_SLOT);
+    } else {
+      const int32_t* m = meta + kvc_meta_row(b);
+      const int chunks = m[KVC_ROW_CHUNKS];
+      const int s = m[KVC_ROW_BASE] + i;
+      const bool ok = chunks > 0 && s >= 0 && s < cap && (layout != KVC_LINEAR || s < m[KVC_ROW_FILLED]);
+      if (ok) drow = (int64_t)b * cap + s;
+      else if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, chunks > 0 ? KVC_DEV_BAD_SLOT : KVC_DEV_NO_CHUNK);
+    }
+    if (drow < 0) continue;
+    const uint4* src = (t ? vsrc : ksrc) + (int64_t)e * row_vecs;
+    uint4* dst = (t ? vdst : kdst) + drow * row_vecs;
+    for (int v0 = lane; v0 < row_vecs; v0 += 32 * kWriteUnroll) {
+      uint4 val[kWriteUnroll];
+#pragma unroll
+      for (int u = 0; u < kWriteUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < row_vecs) val[u] = __ldg(src + v);
+      }
+#pragma unroll
+      for (int u = 0; u < kWriteUnroll; ++u) {
+        const int v = v0 + 32 * u;
+        if (v < row_vecs) dst[v] = val[u];
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t kvc_launch_advance(kvc_cache* c, int row, int n, cudaStream_t s) {
+  const kvc_config& g = c->cfg;
+  k_advance<<<1, 128, 0, s>>>(c->meta, g.batch, row, n, g.layout, g.sink, g.window, g.chunk, c->cap);
+  return cudaGetLastError();
+}
+
+cudaError_t kvc_launch_reset(kvc_cache* c, int row, cudaStream_t s) {
+  k_reset<<<1, 128, 0, s>>>(c->meta, c->cfg.batch, row);
+  return cudaGetLastError();
+}
+
+cudaError_t kvc_launch_set_lengths(kvc_cache* c, const int32_t* kv_len, const int32_t* cu, cudaStream_t s) {
+  k_set_lengths<<<1, 128, 0, s>>>(c->meta, c->cfg.batch, c->cap, kv_len, cu);
+  return cudaGetLastError();
+}
+
+cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
+                             cudaStream_t s) {
+  const kvc_config& g = c->cfg;
+  const int row_vecs = g.kv_heads * g.head_dim * c->eb / 16;
+  const int64_t rows = 2LL * g.batch * n;
+  int64_t blocks = (rows + kWriteThreads / 32 - 1) / (kWriteThreads / 32);
+  const int64_t max_blocks = (int64_t)c->num_sms * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+  k_write<<<(unsigned)blocks, kWriteThreads, 0, s>>>((const uint4*)k, (const uint4*)v, (uint4*)c->k, (uint4*)c->v,
+                                                     c->meta, slots, g.batch, n, row_vecs, c->cap, g.layout);
+  return cudaGetLastError();
+}

@@ -1,0 +1,209 @@
+// C-ABI entry points of libkvc.so (declared and documented in include/kvc.h):
+// host-side validation, handle state and kernel selection.  Every call only
+// enqueues work on the caller's stream; nothing here allocates device memory.
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "kvc_internal.h"
+
+namespace {
+
+// Blocks the split-KV decode kernel aims for (about two per SM of a 152-SM GB300).
+// A constant, so that workspace sizes do not depend on the device queried.
+constexpr int kDecodeTargetBlocks = 304;
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int elem_bytes(int dtype) { return dtype == KVC_F32 ? 4 : 2; }
+
+// Validate a config; on success store the per-row slot count in *cap.
+int check_cfg(const kvc_config* cfg, int* cap) {
+  if (cfg == nullptr) return KVC_ERR_ARG;
+  if (cfg->batch < 1 || cfg->heads < 1 || cfg->kv_heads < 1 || cfg->heads % cfg->kv_heads) return KVC_ERR_ARG;
+  if (cfg->dtype < KVC_F32 || cfg->dtype > KVC_BF16) return KVC_ERR_ARG;
+  if (cfg->head_dim != 64 && cfg->head_dim != 128) return KVC_ERR_UNSUPPORTED;
+  if (!(cfg->softmax_scale >= 0.f) || isinf(cfg->softmax_scale)) return KVC_ERR_ARG;
+  switch (cfg->layout) {
+    case KVC_CIRCULAR:
+      if (cfg->chunk < 1 || cfg->sink < 0 || cfg->window <= cfg->sink) return KVC_ERR_ARG;
+      if (cfg->sink % cfg->chunk || (cfg->window - cfg->sink) % cfg->chunk) return KVC_ERR_ARG;
+      *cap = cfg->window;
+      break;
+    case KVC_LINEAR:
+    case KVC_PACKED:
+      if (cfg->capacity < 1) return KVC_ERR_ARG;
+      *cap = cfg->capacity;
+      break;
+    default:
+      return KVC_ERR_ARG;
+  }
+  // element offsets of the store must fit the kernels' 64-bit arithmetic; row counts
+  // must fit int32
+  const int64_t rows = (int64_t)(cfg->layout == KVC_PACKED ? 1 : cfg->batch) * (*cap);
+  if (rows > INT32_MAX) return KVC_ERR_ARG;
+  return KVC_OK;
+}
+
+int decode_splits(const kvc_config& cfg, int cap) {
+  const int pairs = cfg.batch * cfg.kv_heads;
+  int n = (kDecodeTargetBlocks + pairs - 1) / pairs;
+  const int need = (cap + 2047) / 2048;
+  if (n < need) n = need;
+  if (n > cap) n = cap;
+  return n < 1 ? 1 : n;
+}
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int launched(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t kvc_meta_bytes(const kvc_config* cfg) {
+  int cap = 0;
+  if (check_cfg(cfg, &cap) != KVC_OK) return 0;
+  const size_t words = (size_t)kvc_meta_cu(cfg->batch) + cfg->batch + 1;
+  return (words * 4 + 255) & ~(size_t)255;
+}
+
+size_t kvc_workspace_bytes(const kvc_config* cfg) {
+  int cap = 0;
+  if (check_cfg(cfg, &cap) != KVC_OK) return 0;
+  if (!kvc_decode_supported(*cfg)) return 0;
+  const size_t b = kvc_decode_workspace_bytes(*cfg, decode_splits(*cfg, cap));
+  return (b + 255) & ~(size_t)255;
+}
+
+int kvc_create(const kvc_config* cfg, void* k_store, void* v_store, void* meta, void* workspace, void* stream,
+               kvc_cache** out) {
+  int cap = 0;
+  if (out == nullptr) return KVC_ERR_ARG;
+  *out = nullptr;
+  int rc = check_cfg(cfg, &cap);
+  if (rc != KVC_OK) return rc;
+  if (!k_store || !v_store || !meta || !aligned16(k_store) || !aligned16(v_store) || !aligned16(meta))
+    return KVC_ERR_ARG;
+  const size_t ws_bytes = kvc_workspace_bytes(cfg);
+  if (ws_bytes > 0 && (workspace == nullptr || !aligned16(workspace))) return KVC_ERR_ARG;
+
+  kvc_cache* c = new (std::nothrow) kvc_cache();
+  if (c == nullptr) return KVC_ERR_ARG;
+  c->cfg = *cfg;
+  c->cap = cap;
+  c->eb = elem_bytes(cfg->dtype);
+  c->scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / sqrtf((float)cfg->head_dim);
+  c->k = k_store;
+  c->v = v_store;
+  c->meta = reinterpret_cast<int32_t*>(meta);
+  c->ws = workspace;
+  c->dec_splits = kvc_decode_supported(*cfg) ? decode_splits(*cfg, cap) : 0;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
+    delete c;
+    return KVC_ERR_CUDA;
+  }
+  if (c->dec_splits > 0 && kvc_prepare_decode(c) != cudaSuccess) {
+    delete c;
+    return KVC_ERR_CUDA;
+  }
+  c->tc_ok = kvc_tc_supported(*cfg) && kvc_tc_make_kv_maps(c);
+  cudaStream_t s = as_stream(stream);
+  if (cudaMemsetAsync(meta, 0, kvc_meta_bytes(cfg), s) != cudaSuccess ||
+      (ws_bytes > 0 && cudaMemsetAsync(workspace, 0, ws_bytes, s) != cudaSuccess)) {
+    delete c;
+    return KVC_ERR_CUDA;
+  }
+  *out = c;
+  return KVC_OK;
+}
+
+int kvc_advance(kvc_cache* c, int32_t row, int32_t n_tokens, void* stream) {
+  if (c == nullptr || row >= c->cfg.batch) return KVC_ERR_ARG;
+  switch (c->cfg.layout) {
+    case KVC_CIRCULAR:
+      if (n_tokens != c->cfg.chunk) return KVC_ERR_ARG;
+      break;
+    case KVC_LINEAR:
+      if (n_tokens < 1) return KVC_ERR_ARG;
+      if (n_tokens > c->cap) return KVC_ERR_RANGE;
+      break;
+    default:
+      return KVC_ERR_UNSUPPORTED;
+  }
+  return launched(kvc_launch_advance(c, row < 0 ? -1 : row, n_tokens, as_stream(stream)));
+}
+
+int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, const int32_t* d_slots, void* stream) {
+  if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;
+  if (n_tokens > c->cap) return KVC_ERR_RANGE;
+  if (d_slots != nullptr) {
+    if (c->cfg.layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;
+    if (((uintptr_t)d_slots & 3u) != 0) return KVC_ERR_ARG;
+  } else if (c->cfg.layout == KVC_CIRCULAR && n_tokens != c->cfg.chunk) {
+    return KVC_ERR_ARG;
+  }
+  return launched(kvc_launch_write(c, k, v, n_tokens, d_slots, as_stream(stream)));
+}
+
+int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_seqlens, void* stream) {
+  if (c == nullptr || (d_kv_len == nullptr && d_cu_seqlens == nullptr)) return KVC_ERR_ARG;
+  if (d_kv_len != nullptr && c->cfg.layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;
+  if (d_cu_seqlens != nullptr && c->cfg.layout != KVC_PACKED) return KVC_ERR_UNSUPPORTED;
+  return launched(kvc_launch_set_lengths(c, d_kv_len, d_cu_seqlens, as_stream(stream)));
+}
+
+int kvc_attend(kvc_cache* c, const void* q, void* out, int32_t n_q, uint32_t flags, void* stream) {
+  if (c == nullptr || !q || !out || !aligned16(q) || !aligned16(out) || n_q < 1) return KVC_ERR_ARG;
+  if (flags & ~(uint32_t)(KVC_CAUSAL | KVC_KERNEL_SIMT)) return KVC_ERR_ARG;
+  const bool causal = (flags & KVC_CAUSAL) != 0;
+  if (causal && c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
+  cudaStream_t s = as_stream(stream);
+  if ((flags & KVC_KERNEL_SIMT) || c->cfg.dtype == KVC_F32) return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, s));
+  if (n_q == 1 && c->dec_splits > 0) return launched(kvc_launch_decode(c, q, out, s));
+  if (c->tc_ok) return launched(kvc_launch_attn_tc(c, q, out, n_q, causal, s));
+  return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, s));
+}
+
+int kvc_reset(kvc_cache* c, int32_t row, void* stream) {
+  if (c == nullptr || row >= c->cfg.batch) return KVC_ERR_ARG;
+  return launched(kvc_launch_reset(c, row < 0 ? -1 : row, as_stream(stream)));
+}
+
+int kvc_get_error(kvc_cache* c, void* stream, int32_t* bits) {
+  if (c == nullptr) return KVC_ERR_ARG;
+  cudaStream_t s = as_stream(stream);
+  int32_t word = 0;
+  if (cudaMemcpyAsync(&word, c->meta + KVC_META_ERR, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  if (bits != nullptr) *bits = word;
+  if (word == 0) return KVC_OK;
+  if (cudaMemsetAsync(c->meta + KVC_META_ERR, 0, sizeof(int32_t), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return KVC_ERR_DEVICE;
+}
+
+int kvc_destroy(kvc_cache* c) {
+  delete c;
+  return KVC_OK;
+}
+
+const char* kvc_strerror(int code) {
+  switch (code) {
+    case KVC_OK: return "ok";
+    case KVC_ERR_ARG: return "invalid argument";
+    case KVC_ERR_UNSUPPORTED: return "unsupported configuration or request";
+    case KVC_ERR_RANGE: return "length out of range";
+    case KVC_ERR_CUDA: return "CUDA error";
+    case KVC_ERR_DEVICE: return "device-side error reported";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// Internal declarations shared by the kvc host layer and its kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvc.h"
+
+// ---- meta block layout (int32 words; documented in kvc.h) -------------------
+#define KVC_META_ERR 0
+#define KVC_META_ROW0 4
+#define KVC_ROW_CHUNKS 0   // chunks reserved so far
+#define KVC_ROW_BASE 1     // first slot of the reserved chunk
+#define KVC_ROW_FILLED 2   // slots filled (end of the reservation for LINEAR)
+#define KVC_ROW_KVLEN 3    // active prefix attended by kvc_attend
+__host__ __device__ inline int kvc_meta_row(int b) { return KVC_META_ROW0 + 4 * b; }
+__host__ __device__ inline int kvc_meta_cu(int B) { return KVC_META_ROW0 + 4 * B; }
+
+struct kvc_cache {
+  kvc_config cfg;
+  int cap;            // slots per row (LINEAR capacity, CIRCULAR window) or packed total
+  int eb;             // element bytes
+  float scale;        // softmax scale
+  void* k;
+  void* v;
+  int32_t* meta;
+  void* ws;
+  int device;
+  int num_sms;
+  int dec_splits;     // split-KV decode: splits per (row, kv head); 0 = no decode kernel
+  bool tc_ok;         // the tensor-core chunk kernel serves this config
+  CUtensorMap tm_k;   // K store, 128B-swizzled 64x128 boxes (tensor-core kernel)
+  CUtensorMap tm_v;   // V store, same boxes
+};
+
+// Row geometry of the store as seen by the attention kernels: row b's slot j lives
+// at element ((b * row_stride_b) + (row0_b + j)) * Hkv * D + kvh * D.  For LINEAR
+// and CIRCULAR row0_b = 0 and row_stride_b = cap; for PACKED row_stride_b = 0 and
+// row0_b = cu_seqlens[b].
+struct kvc_geom {
+  int B, H, Hkv, D, cap, layout;
+};
+
+// Valid slot range of row b read from the meta block on the device.  Returns false
+// (and sets the error word) when the row's length is out of range.
+__device__ __forceinline__ bool kvc_row_range(const int32_t* meta, const kvc_geom& g, int b,
+                                              int* row0, int* len, int32_t* err_word) {
+  if (g.layout == KVC_PACKED) {
+    const int32_t* cu = meta + kvc_meta_cu(g.B);
+    int lo = cu[b], hi = cu[b + 1];
+    if (lo < 0 || hi <= lo || hi > g.cap) {
+      atomicOr(err_word, KVC_DEV_BAD_CUSEQ);
+      return false;
+    }
+    *row0 = lo;
+    *len = hi - lo;
+    return true;
+  }
+  int n = meta[kvc_meta_row(b) + KVC_ROW_KVLEN];
+  if (n < 1 || n > g.cap) {
+    atomicOr(err_word, KVC_DEV_BAD_KVLEN);
+    return false;
+  }
+  *row0 = 0;
+  *len = n;
+  return true;
+}
+
+// Element offset of (row b, slot j, kv head kvh, dim 0).
+__device__ __forceinline__ int64_t kvc_kv_offset(const kvc_geom& g, int b, int row0, int j, int kvh) {
+  int64_t row = (g.layout == KVC_PACKED) ? (int64_t)(row0 + j) : (int64_t)b * g.cap + (row0 + j);
+  return (row * g.Hkv + kvh) * (int64_t)g.D;
+}
+
+// ---- launchers (each returns a cudaError_t from the launch) ------------------
+cudaError_t kvc_launch_advance(kvc_cache* c, int row, int n, cudaStream_t s);
+cudaError_t kvc_launch_reset(kvc_cache* c, int row, cudaStream_t s);
+cudaError_t kvc_launch_set_lengths(kvc_cache* c, const int32_t* kv_len, const int32_t* cu, cudaStream_t s);
+cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
+                             cudaStream_t s);
+cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
+                                 cudaStream_t s);
+cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s);
+cudaError_t kvc_prepare_decode(kvc_cache* c);
+bool kvc_decode_supported(const kvc_config& cfg);
+size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits);
+cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
+                               cudaStream_t s);
+bool kvc_tc_supported(const kvc_config& cfg);
+bool kvc_tc_make_kv_maps(kvc_cache* c);

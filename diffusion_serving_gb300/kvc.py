@@ -1,0 +1,228 @@
+"""Python binding of libkvc.so (include/kvc.h): argument marshalling only.
+
+The functions below carry the C names and take torch tensors (device memory) and
+torch CUDA streams; they pass raw pointers to the library and raise ``KvcError``
+on a non-zero return code.  Every step of the computation runs in the library's
+CUDA kernels.  ``KVCache`` bundles a handle with torch-allocated buffers.
+
+Importing this module loads libkvc.so and fails loudly if it has not been built
+(``python -m diffusion_serving_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "kvc.h")
+
+F32, F16, BF16 = 0, 1, 2
+LINEAR, CIRCULAR, PACKED = 0, 1, 2
+CAUSAL, KERNEL_SIMT = 1, 256
+OK, ERR_ARG, ERR_UNSUPPORTED, ERR_RANGE, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5
+DEV_BAD_SLOT, DEV_BAD_KVLEN, DEV_BAD_CUSEQ, DEV_OVERFLOW, DEV_NO_CHUNK, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
+META_ROW0 = 4
+
+DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+CODE_DTYPE = {v: k for k, v in DTYPE_CODE.items()}
+LAYOUT_CODE = {"linear": LINEAR, "circular": CIRCULAR, "packed": PACKED}
+
+
+class KvcError(RuntimeError):
+    def __init__(self, code: int, what: str, bits: int = 0):
+        self.code, self.bits = code, bits
+        super().__init__(f"{what}: {kvc_strerror(code)} ({code})" + (f", device bits {bits:#x}" if bits else ""))
+
+
+class kvc_config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("sink", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("chunk", ctypes.c_int32), ("capacity", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libkvc.so is not built ({LIB_PATH}); run python -m diffusion_serving_gb300.build")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, U32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
+    cfgp = ctypes.POINTER(kvc_config)
+    sig = {
+        "kvc_meta_bytes": (SZ, [cfgp]),
+        "kvc_workspace_bytes": (SZ, [cfgp]),
+        "kvc_create": (ctypes.c_int, [cfgp, P, P, P, P, P, ctypes.POINTER(P)]),
+        "kvc_advance": (ctypes.c_int, [P, I32, I32, P]),
+        "kvc_write": (ctypes.c_int, [P, P, P, I32, P, P]),
+        "kvc_set_lengths": (ctypes.c_int, [P, P, P, P]),
+        "kvc_attend": (ctypes.c_int, [P, P, P, I32, U32, P]),
+        "kvc_reset": (ctypes.c_int, [P, I32, P]),
+        "kvc_get_error": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
+        "kvc_destroy": (ctypes.c_int, [P]),
+        "kvc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype, fn.argtypes = res, args
+    return lib
+
+
+_lib = _load()
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/kvc.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(kvc_\w+)\s*\(", text, flags=re.M)
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+# ---------------------------------------------------------------------------
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise KvcError(rc, what)
+
+
+def make_config(batch, heads, kv_heads, head_dim, dtype, layout, *, sink=0, window=0, chunk=0,
+                capacity=0, softmax_scale=0.0) -> kvc_config:
+    d = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    lay = LAYOUT_CODE[layout] if isinstance(layout, str) else int(layout)
+    return kvc_config(batch, heads, kv_heads, head_dim, sink, window, chunk, capacity, d, lay, softmax_scale)
+
+
+# ---------------------------------------------------------------------------
+# the C entry points, same names
+# ---------------------------------------------------------------------------
+def kvc_meta_bytes(cfg: kvc_config) -> int:
+    return _lib.kvc_meta_bytes(ctypes.byref(cfg))
+
+
+def kvc_workspace_bytes(cfg: kvc_config) -> int:
+    return _lib.kvc_workspace_bytes(ctypes.byref(cfg))
+
+
+def kvc_create(cfg: kvc_config, k_store, v_store, meta, workspace=None, stream=None) -> int:
+    h = ctypes.c_void_p()
+    _check(_lib.kvc_create(ctypes.byref(cfg), _ptr(k_store), _ptr(v_store), _ptr(meta), _ptr(workspace),
+                           _stream(stream), ctypes.byref(h)), "kvc_create")
+    return h.value
+
+
+def kvc_advance(h: int, row: int = -1, n_tokens: int = 0, stream=None) -> None:
+    _check(_lib.kvc_advance(h, row, n_tokens, _stream(stream)), "kvc_advance")
+
+
+def kvc_write(h: int, k, v, n_tokens: int, slots=None, stream=None) -> None:
+    _check(_lib.kvc_write(h, _ptr(k), _ptr(v), n_tokens, _ptr(slots), _stream(stream)), "kvc_write")
+
+
+def kvc_set_lengths(h: int, kv_len=None, cu_seqlens=None, stream=None) -> None:
+    _check(_lib.kvc_set_lengths(h, _ptr(kv_len), _ptr(cu_seqlens), _stream(stream)), "kvc_set_lengths")
+
+
+def kvc_attend(h: int, q, out, n_q: int, flags: int = 0, stream=None) -> None:
+    _check(_lib.kvc_attend(h, _ptr(q), _ptr(out), n_q, flags, _stream(stream)), "kvc_attend")
+
+
+def kvc_reset(h: int, row: int = -1, stream=None) -> None:
+    _check(_lib.kvc_reset(h, row, _stream(stream)), "kvc_reset")
+
+
+def kvc_get_error(h: int, stream=None) -> int:
+    """Return the device error bits (0 if none) and clear them."""
+    bits = ctypes.c_int32(0)
+    rc = _lib.kvc_get_error(h, _stream(stream), ctypes.byref(bits))
+    if rc not in (OK, ERR_DEVICE):
+        raise KvcError(rc, "kvc_get_error")
+    return bits.value
+
+
+def kvc_destroy(h: int) -> None:
+    _check(_lib.kvc_destroy(h), "kvc_destroy")
+
+
+def kvc_strerror(code: int) -> str:
+    return _lib.kvc_strerror(code).decode()
+
+
+# ---------------------------------------------------------------------------
+# convenience owner of the device buffers
+# ---------------------------------------------------------------------------
+class KVCache:
+    """A kvc handle plus torch-allocated K/V stores, meta block and workspace."""
+
+    def __init__(self, batch, heads, kv_heads, head_dim, dtype, layout, *, sink=0, window=0, chunk=0,
+                 capacity=0, softmax_scale=0.0, device="cuda", stream=None):
+        self.cfg = make_config(batch, heads, kv_heads, head_dim, dtype, layout, sink=sink, window=window,
+                               chunk=chunk, capacity=capacity, softmax_scale=softmax_scale)
+        self.dtype = dtype
+        self.layout = LAYOUT_CODE[layout] if isinstance(layout, str) else int(layout)
+        slots = window if self.layout == CIRCULAR else capacity
+        shape = (slots, kv_heads, head_dim) if self.layout == PACKED else (batch, slots, kv_heads, head_dim)
+        self.k_store = torch.empty(shape, dtype=dtype, device=device)
+        self.v_store = torch.empty(shape, dtype=dtype, device=device)
+        mb = kvc_meta_bytes(self.cfg)
+        if mb == 0:
+            raise KvcError(ERR_ARG, "kvc_meta_bytes")
+        self.meta = torch.zeros(mb // 4, dtype=torch.int32, device=device)
+        wb = kvc_workspace_bytes(self.cfg)
+        self.workspace = torch.zeros(max(wb, 16) // 4, dtype=torch.int32, device=device)
+        self.handle = kvc_create(self.cfg, self.k_store, self.v_store, self.meta, self.workspace, stream)
+
+    def advance(self, row=-1, n_tokens=None, stream=None):
+        kvc_advance(self.handle, row, self.cfg.chunk if n_tokens is None else n_tokens, stream)
+
+    def write(self, k, v, slots=None, stream=None):
+        kvc_write(self.handle, k, v, k.shape[1], slots, stream)
+
+    def set_lengths(self, kv_len=None, cu_seqlens=None, stream=None):
+        kvc_set_lengths(self.handle, kv_len, cu_seqlens, stream)
+
+    def attend(self, q, out=None, flags=0, stream=None):
+        if out is None:
+            out = torch.empty_like(q)
+        kvc_attend(self.handle, q, out, q.shape[1], flags, stream)
+        return out
+
+    def reset(self, row=-1, stream=None):
+        kvc_reset(self.handle, row, stream)
+
+    def get_error(self, stream=None) -> int:
+        return kvc_get_error(self.handle, stream)
+
+    def row_state(self):
+        """(chunks, first slot, filled, kv_len) per row, read from the meta block."""
+        m = self.meta[META_ROW0:META_ROW0 + 4 * self.cfg.batch].view(self.cfg.batch, 4)
+        return m.cpu().tolist()
+
+    def close(self):
+        if self.handle:
+            kvc_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

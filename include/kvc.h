@@ -1,0 +1,191 @@
+/*
+ * kvc.h — attention of a query chunk or a decode token over a device-resident
+ * KV cache, on one NVIDIA GB300 (sm_103a).  C ABI of libkvc.so.
+ *
+ * Sources of the operations (web pages; cited by title and section):
+ *  [IDX]  lingbot-world PR "refactor(kv): index_copy_ for KV-cache writes" —
+ *         Summary; "What this is and isn't" (homogeneous multi-user batching,
+ *         CUDA Graphs).
+ *  [RING] flashdreams issue "add an opt-in circular KV policy for streaming
+ *         attention" — "current path", "proposed boundary", "first experiment".
+ *  [PFX]  fish-speech PR "perf(text2semantic): pass only active KV cache prefix
+ *         to SDPA" — "Problem", "Change", the regression-test reply.
+ *  [VAR]  TensorRT-LLM PR "FA4 variable-length cross-attention" — Description,
+ *         "Microbenchmark, cross-attention op only".
+ *
+ * Conventions shared by every entry point
+ *  - All pointers named d_* or documented "device" are device pointers; every
+ *    tensor pointer must be 16-byte aligned.  Tensors are dense row-major:
+ *      queries / outputs   q, out   [B, n, H, D]
+ *      written K / V rows  k, v     [B, n, Hkv, D]
+ *      LINEAR / CIRCULAR store      [B, cap, Hkv, D]   (cap = capacity or window)
+ *      PACKED store                 [total, Hkv, D]    (row b at cu_seqlens[b])
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    only enqueues work on it; none reads device data back on the host, so the
+ *    advance / write / attend sequence can be captured in a CUDA graph once and
+ *    replayed [RING "proposed boundary", IDX item 2].  kvc_get_error is the one
+ *    call that synchronises.
+ *  - Ownership: the caller owns and allocates every device buffer (K/V store,
+ *    meta block, workspace, inputs, outputs).  The library allocates no device
+ *    memory; it owns only the host-side handle.  Buffers must outlive the handle.
+ *  - Return value: 0 on success, a negative KVC_ERR_* code otherwise.  Host-side
+ *    validation failures enqueue nothing.  Errors found on the device (a slot,
+ *    length or offset out of range) never fault: the kernel skips the offending
+ *    row, sets a bit in the meta block's error word, and kvc_get_error reports it.
+ */
+#ifndef KVC_H_
+#define KVC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  F32 attention runs in true fp32 FMA arithmetic; F16/BF16 run the
+ * contractions on the tensor cores with fp32 accumulation.  Outputs have the
+ * input type. */
+typedef enum { KVC_F32 = 0, KVC_F16 = 1, KVC_BF16 = 2 } kvc_dtype;
+
+/* Store layouts.
+ *  LINEAR   capacity slots per row, active prefix kv_len [PFX "Change"].
+ *  CIRCULAR sink + rolling window of whole chunks, attended in physical order
+ *           [RING "proposed boundary"]; `window` counts the sink.
+ *  PACKED   ragged per-row K/V back to back, offsets cu_seqlens [VAR Description]. */
+typedef enum { KVC_LINEAR = 0, KVC_CIRCULAR = 1, KVC_PACKED = 2 } kvc_layout;
+
+typedef struct kvc_config {
+  int32_t batch;       /* B rows (users / CFG branches), each with its own state   */
+  int32_t heads;       /* H query heads                                            */
+  int32_t kv_heads;    /* Hkv; H % Hkv == 0, q-head h reads kv-head h / (H/Hkv)     */
+  int32_t head_dim;    /* D: 64 or 128                                             */
+  int32_t sink;        /* CIRCULAR: pinned sink tokens, a multiple of chunk (may be 0) */
+  int32_t window;      /* CIRCULAR: total slots incl. sink, sink + a multiple of chunk */
+  int32_t chunk;       /* CIRCULAR: tokens per chunk                               */
+  int32_t capacity;    /* LINEAR: slots per row; PACKED: total packed slots         */
+  int32_t dtype;       /* kvc_dtype                                                */
+  int32_t layout;      /* kvc_layout                                               */
+  float softmax_scale; /* 0 => 1/sqrt(head_dim), the SDPA default                  */
+} kvc_config;
+
+typedef struct kvc_cache kvc_cache;
+
+enum {
+  KVC_OK = 0,
+  KVC_ERR_ARG = -1,         /* null / misaligned pointer, bad shape or config       */
+  KVC_ERR_UNSUPPORTED = -2, /* a valid request this library does not serve, e.g.
+                               causal attention over a circular store [RING]       */
+  KVC_ERR_RANGE = -3,       /* a host-known length out of range [PFX tests item 2] */
+  KVC_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed                */
+  KVC_ERR_DEVICE = -5       /* kvc_get_error: the device error word was non-zero   */
+};
+
+/* Bits of the device error word (meta word 0), reported by kvc_get_error. */
+enum {
+  KVC_DEV_BAD_SLOT = 1,     /* a d_slots entry outside [0, cap)                     */
+  KVC_DEV_BAD_KVLEN = 2,    /* a kv_len outside [1, cap] at attend / set_lengths   */
+  KVC_DEV_BAD_CUSEQ = 4,    /* cu_seqlens not increasing from 0 or beyond capacity  */
+  KVC_DEV_OVERFLOW = 8,     /* LINEAR advance past capacity                         */
+  KVC_DEV_NO_CHUNK = 16,    /* write with no reserved chunk                         */
+  KVC_DEV_TIMEOUT = 32      /* a bounded in-kernel wait gave up (the kernel returned) */
+};
+
+/* Attention flags. */
+enum {
+  KVC_CAUSAL = 1,           /* LINEAR only: query i at position kv_len - n_q + i sees
+                               keys at positions <= its own [PFX "Change"]          */
+  KVC_KERNEL_SIMT = 256     /* run the fp32-FMA kernel for any dtype (a cross-check
+                               of the tensor-core and decode kernels)               */
+};
+
+/* Meta block: int32 words, device memory owned by the caller.
+ *   [0] error word  [1..3] reserved
+ *   [4 + 4b + 0] chunks reserved by row b   [4 + 4b + 1] first slot of its chunk
+ *   [4 + 4b + 2] slots filled               [4 + 4b + 3] kv_len (active prefix)
+ *   [4 + 4B + b], b = 0..B: cu_seqlens (PACKED)
+ * kvc_create initialises it. */
+size_t kvc_meta_bytes(const kvc_config* cfg);
+
+/* Device scratch for the split-KV decode kernel (partial outputs and their
+ * log-sum-exp terms, plus per-(row, kv-head) tickets that each call leaves at zero).
+ * Zero for a config with nothing to split.  Caller-allocated, passed to kvc_create. */
+size_t kvc_workspace_bytes(const kvc_config* cfg);
+
+/* Create a handle over caller-owned device buffers.
+ *  k_store, v_store: the K and V stores (layouts above), any prior contents.
+ *  meta: kvc_meta_bytes(cfg) bytes; workspace: kvc_workspace_bytes(cfg) bytes
+ *  (NULL allowed when that is 0).  Enqueues the meta initialisation on `stream`:
+ *  every row empty, no chunk reserved, error word 0.
+ *  Errors: KVC_ERR_ARG for a bad config or pointer, KVC_ERR_UNSUPPORTED for an
+ *  unsupported head_dim or dtype, KVC_ERR_CUDA. */
+int kvc_create(const kvc_config* cfg, void* k_store, void* v_store, void* meta,
+               void* workspace, void* stream, kvc_cache** out);
+
+/* Reserve the next chunk of `row` (all rows when row < 0) [RING "proposed
+ * boundary": reservation separate from writes, so denoising rewrites replace the
+ * same chunk].
+ *  CIRCULAR: n_tokens must equal `chunk`.  Chunk k's first slot is k*chunk while
+ *    the ring fills, then sink + ((k - sink/chunk) mod ((window-sink)/chunk))*chunk:
+ *    the oldest rolling chunk is evicted, the sink stays pinned [RING "current
+ *    path"].  kv_len = min((k+1)*chunk, window).
+ *  LINEAR: reserves n_tokens slots after those filled; kv_len = slots filled.  Past
+ *    capacity sets KVC_DEV_OVERFLOW and leaves the row unchanged.
+ *  PACKED: KVC_ERR_UNSUPPORTED (lengths come from kvc_set_lengths). */
+int kvc_advance(kvc_cache* c, int32_t row, int32_t n_tokens, void* stream);
+
+/* Write n_tokens rows of K and V (device, [B, n_tokens, Hkv, D]) into the store,
+ * the index_copy-style write of [IDX Summary].
+ *  d_slots == NULL: row b's token i goes to its reserved chunk (first slot from the
+ *    meta block, so a replayed graph writes the slot the device holds [RING]); for
+ *    PACKED to cu_seqlens[b] + i for i < len_b (the pack of [VAR]), tokens past
+ *    len_b are ignored.
+ *  d_slots != NULL (device int32[n_tokens]): token i of every row goes to slot
+ *    d_slots[i] — one index shared by all rows on the same timeline [IDX item 1].
+ *    Not for PACKED.  Entries outside [0, cap) set KVC_DEV_BAD_SLOT and are skipped.
+ * Bytes are copied unchanged (bit-exact). */
+int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
+              const int32_t* d_slots, void* stream);
+
+/* Set lengths from device arrays (either may be NULL).
+ *  d_kv_len (int32[B]): LINEAR / CIRCULAR active prefix per row [PFX "Change"; the
+ *    per-row used length of a padded store in VAR].  Values outside [1, cap] set
+ *    KVC_DEV_BAD_KVLEN and leave that row's kv_len unchanged.
+ *  d_cu_seqlens (int32[B+1]): PACKED offsets [VAR Description]; must start at 0,
+ *    increase strictly and end <= capacity, else KVC_DEV_BAD_CUSEQ and nothing is
+ *    changed.  Sets each row's kv_len to its length. */
+int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_seqlens,
+                    void* stream);
+
+/* out[b, i, h, :] = sum_j softmax_j(scale * q[b,i,h,:] . k_j) v_j over row b's
+ * valid slots, read in physical order with no gather or roll (unmasked attention
+ * is invariant to permuting K and V rows together [RING "proposed boundary"]).
+ * Valid slots: [0, kv_len_b) for LINEAR and CIRCULAR, [cu_b, cu_{b+1}) for PACKED;
+ * nothing past them is read into the result [PFX "Change"].
+ *  q (device [B, n_q, H, D]), out (device, same shape and dtype).
+ *  flags: KVC_CAUSAL (LINEAR only, else KVC_ERR_UNSUPPORTED), KVC_KERNEL_SIMT.
+ *  A row whose kv_len is outside [1, cap] at run time gets KVC_DEV_BAD_KVLEN and
+ *  its output is left unwritten. */
+int kvc_attend(kvc_cache* c, const void* q, void* out, int32_t n_q, uint32_t flags,
+               void* stream);
+
+/* Forget the contents of `row` (all rows when row < 0): no chunk reserved, nothing
+ * filled, kv_len 0; storage bytes are left as they are [RING "proposed boundary"
+ * reset semantics]. */
+int kvc_reset(kvc_cache* c, int32_t row, void* stream);
+
+/* Synchronise `stream`, then return KVC_ERR_DEVICE if the device error word is
+ * non-zero (its bits are stored in *bits when bits != NULL) and clear it; KVC_OK
+ * otherwise. */
+int kvc_get_error(kvc_cache* c, void* stream, int32_t* bits);
+
+/* Free the host handle.  Device buffers stay with the caller. */
+int kvc_destroy(kvc_cache* c);
+
+/* Static string for a return code. */
+const char* kvc_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVC_H_ */

@@ -1,0 +1,200 @@
+"""GPU tests of slot reservation, writes, lengths and device-side error reporting.
+
+The cache contents must be bit-exact against the oracle's chronological history read
+through its closed-form slot map (flashdreams issue "add an opt-in circular KV
+policy for streaming attention", "first experiment"), and a device-index write must
+equal torch slice-assignment (lingbot-world PR "refactor(kv): index_copy_ for
+KV-cache writes", "Verification").
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from diffusion_serving_gb300 import kvc
+
+
+def bits(t):
+    return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+def store_matches_history(cache, oracle, b, dtype):
+    """Every attended position of row b sits, bit-exact, at its closed-form slot."""
+    pos = oracle.attended_positions(b)
+    slots = torch.tensor([oracle.physical_slot(b, p) for p in pos], device="cuda")
+    for store, hist in ((cache.k_store, oracle.hist_k[b]), (cache.v_store, oracle.hist_v[b])):
+        want = torch.from_numpy(np.stack([hist[p] for p in pos])).to(dtype)
+        got = store[b].index_select(0, slots).cpu()
+        if not torch.equal(bits(got), bits(want)):
+            return False
+    return True
+
+
+@pytest.mark.parametrize("chunk,sink_c,roll_c", [(4, 1, 3), (2, 0, 4), (1, 3, 2), (4, 2, 1)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ring_fill_rewrite_wrap_reset_bit_exact(chunk, sink_c, roll_c, dtype):
+    B, Hkv, D = 2, 2, 64
+    sink, window = sink_c * chunk, (sink_c + roll_c) * chunk
+    cache = kvc.KVCache(B, Hkv, Hkv, D, dtype, "circular", sink=sink, window=window, chunk=chunk)
+    oracle = orc.ChronoCache(B, Hkv, D, orc.CIRCULAR, sink=sink, window=window, chunk=chunk)
+    g = torch.Generator().manual_seed(5)
+    n_chunks = sink_c + 2 * roll_c + 2
+    for rnd in range(2):
+        for c in range(n_chunks):
+            cache.advance()
+            oracle.advance()
+            for rw in range(2):
+                k = torch.randn(B, chunk, Hkv, D, generator=g).to(dtype)
+                v = torch.randn(B, chunk, Hkv, D, generator=g).to(dtype)
+                cache.write(k.cuda(), v.cuda())
+                oracle.write(k.double().numpy(), v.double().numpy())
+                for b in range(B):
+                    assert store_matches_history(cache, oracle, b, dtype)
+                state = cache.row_state()
+                for b in range(B):
+                    assert state[b][3] == len(oracle.attended_positions(b))
+        cache.reset()
+        oracle.reset()
+        assert all(r == [0, 0, 0, 0] for r in cache.row_state())
+    assert cache.get_error() == 0
+
+
+@pytest.mark.parametrize("B", [1, 2])
+def test_index_write_equals_slice_assign(B):
+    """Writes at a device index tensor equal slice-assignment, 7 chunks."""
+    H, D, C, cap = 4, 128, 5, 64
+    cache = kvc.KVCache(B, H, H, D, torch.bfloat16, "linear", capacity=cap)
+    ref_k = torch.zeros(B, cap, H, D, dtype=torch.bfloat16, device="cuda")
+    ref_v = torch.zeros_like(ref_k)
+    cache.k_store.zero_()
+    cache.v_store.zero_()
+    idx = torch.empty(C, dtype=torch.int32, device="cuda")
+    for c in range(7):
+        k = torch.randn(B, C, H, D, device="cuda").to(torch.bfloat16)
+        v = torch.randn(B, C, H, D, device="cuda").to(torch.bfloat16)
+        idx.copy_(torch.arange(c * C, (c + 1) * C, dtype=torch.int32))
+        cache.write(k, v, slots=idx)
+        ref_k[:, c * C:(c + 1) * C] = k
+        ref_v[:, c * C:(c + 1) * C] = v
+        assert torch.equal(bits(cache.k_store), bits(ref_k))
+        assert torch.equal(bits(cache.v_store), bits(ref_v))
+    assert cache.get_error() == 0
+
+
+def test_linear_advance_progression_and_overflow():
+    """kv_len follows prefill T then T+1, T+2 ...; advancing past capacity is reported."""
+    cache = kvc.KVCache(1, 2, 2, 64, torch.float16, "linear", capacity=8)
+    cache.advance(n_tokens=3)
+    seen = [cache.row_state()[0][3]]
+    for _ in range(2):
+        cache.advance(n_tokens=1)
+        seen.append(cache.row_state()[0][3])
+    assert seen == [3, 4, 5]
+    cache.advance(n_tokens=3)
+    assert cache.row_state()[0][3] == 8
+    assert cache.get_error() == 0
+    cache.advance(n_tokens=1)
+    assert cache.get_error() == kvc.DEV_OVERFLOW
+    assert cache.row_state()[0][3] == 8
+
+
+def test_kv_len_bounds_on_device():
+    """kv_len 1 and capacity are accepted, 0 and capacity + 1 rejected."""
+    cache = kvc.KVCache(1, 2, 2, 64, torch.float16, "linear", capacity=8)
+    for n, ok in ((1, True), (8, True), (0, False), (9, False)):
+        cache.set_lengths(kv_len=torch.tensor([n], dtype=torch.int32, device="cuda"))
+        err = cache.get_error()
+        assert (err == 0) == ok, (n, err)
+    with pytest.raises(kvc.KvcError):
+        cache.advance(n_tokens=9)
+
+
+def test_bad_slots_and_cu_seqlens_are_reported_not_faulted():
+    cache = kvc.KVCache(2, 2, 2, 64, torch.bfloat16, "linear", capacity=16)
+    before = cache.k_store.clone()
+    k = torch.randn(2, 3, 2, 64, device="cuda").to(torch.bfloat16)
+    cache.write(k, k, slots=torch.tensor([0, 16, -1], dtype=torch.int32, device="cuda"))
+    assert cache.get_error() == kvc.DEV_BAD_SLOT
+    assert torch.equal(bits(cache.k_store[:, 0]), bits(k[:, 0]))
+    assert torch.equal(bits(cache.k_store[:, 1:]), bits(before[:, 1:]))
+    # write before any reservation
+    cache.write(k, k)
+    assert cache.get_error() == kvc.DEV_NO_CHUNK
+    # attend with kv_len 0 leaves the output untouched and reports
+    q = torch.randn(2, 4, 2, 64, device="cuda").to(torch.bfloat16)
+    out = torch.full_like(q, 7.0)
+    cache.attend(q, out)
+    assert cache.get_error() & kvc.DEV_BAD_KVLEN
+    assert torch.all(out == 7.0)
+    packed = kvc.KVCache(2, 2, 2, 64, torch.bfloat16, "packed", capacity=16)
+    for cu in ([0, 5, 4], [1, 3, 5], [0, 8, 17], [0, 0, 3]):
+        packed.set_lengths(cu_seqlens=torch.tensor(cu, dtype=torch.int32, device="cuda"))
+        assert packed.get_error() == kvc.DEV_BAD_CUSEQ, cu
+
+
+def test_host_validation():
+    with pytest.raises(kvc.KvcError):
+        kvc.KVCache(1, 3, 2, 64, torch.float16, "linear", capacity=8)          # H % Hkv
+    with pytest.raises(kvc.KvcError):
+        kvc.KVCache(1, 2, 2, 64, torch.float16, "circular", sink=3, window=16, chunk=4)
+    ring = kvc.KVCache(1, 2, 2, 64, torch.float16, "circular", sink=4, window=16, chunk=4)
+    q = torch.randn(1, 4, 2, 64, device="cuda").half()
+    with pytest.raises(kvc.KvcError) as e:
+        ring.attend(q, flags=kvc.CAUSAL)
+    assert e.value.code == kvc.ERR_UNSUPPORTED
+    with pytest.raises(kvc.KvcError):
+        ring.advance(n_tokens=3)
+    with pytest.raises(kvc.KvcError):
+        ring.write(q[:, :3, :, :], q[:, :3, :, :])
+
+
+def test_graph_replay_writes_the_device_slot():
+    """A captured advance+write+attend replayed per chunk equals the eager run and
+    writes a different slot each chunk (flashdreams issue, "proposed boundary")."""
+    B, H, D, C, S, W = 2, 4, 128, 8, 8, 40
+    n_chunks = 9
+    ins = [tuple(torch.randn(B, C, H, D, device="cuda").to(torch.bfloat16) for _ in range(3))
+           for _ in range(n_chunks)]
+    eager = kvc.KVCache(B, H, H, D, torch.bfloat16, "circular", sink=S, window=W, chunk=C)
+    eager_out = []
+    for q, k, v in ins:
+        eager.advance()
+        eager.write(k, v)
+        eager_out.append(eager.attend(q))
+    torch.cuda.synchronize()
+
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        cache = kvc.KVCache(B, H, H, D, torch.bfloat16, "circular", sink=S, window=W, chunk=C)
+        qb, kb, vb = (torch.empty_like(x) for x in ins[0])
+        ob = torch.empty_like(qb)
+        # warm-up outside capture: chunk 0
+        qb.copy_(ins[0][0]); kb.copy_(ins[0][1]); vb.copy_(ins[0][2])
+        cache.advance(stream=side)
+        cache.write(kb, vb, stream=side)
+        cache.attend(qb, ob, stream=side)
+    side.synchronize()
+    outs = [ob.clone()]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        cache.advance(stream=side)
+        cache.write(kb, vb, stream=side)
+        cache.attend(qb, ob, stream=side)
+    bases = []
+    for c in range(1, n_chunks):
+        qb.copy_(ins[c][0]); kb.copy_(ins[c][1]); vb.copy_(ins[c][2])
+        graph.replay()
+        torch.cuda.synchronize()
+        outs.append(ob.clone())
+        bases.append(cache.row_state()[0][1])
+    for a, b in zip(outs, eager_out):
+        assert torch.equal(bits(a), bits(b))
+    # every slot was written by now: the stores agree bit for bit
+    assert torch.equal(bits(cache.k_store), bits(eager.k_store))
+    assert torch.equal(bits(cache.v_store), bits(eager.v_store))
+    assert bases == [8, 16, 24, 32, 8, 16, 24, 32]
+    assert cache.get_error() == 0 and eager.get_error() == 0
