@@ -1,8 +1,580 @@
-// Tensor-core chunk attention (placeholder until the tcgen05 kernel lands).
+// Tensor-core chunk attention for bf16 / fp16, D = 128 (sm_103a: tcgen05 + TMEM + TMA).
+//
+// Computes, for every query row of a chunk, softmax(scale * q K^T) V over the row's
+// valid slots in physical order: [0, kv_len) of a LINEAR or CIRCULAR store (the
+// circular sink+window ring is attended as stored, since permuting K and V rows
+// together leaves unmasked attention unchanged — flashdreams issue "add an opt-in
+// circular KV policy for streaming attention", "proposed boundary"), or
+// [cu_b, cu_{b+1}) of a PACKED store (TensorRT-LLM PR "FA4 variable-length
+// cross-attention", Description).  Only the active prefix is read (fish-speech PR
+// "pass only active KV cache prefix to SDPA", "Change"); with KVC_CAUSAL the query
+// at absolute position kv_len - n_q + i sees slots <= that position (same section).
+//
+// One CTA = two 128-row query tiles (A and B) of one (batch row, q head), sharing every
+// K/V tile it loads.  Warp roles (384 threads):
+//   warp 0      TMA producer: Q tiles once, then K and V tiles of 128 slots into a
+//               two-stage ring (128B-swizzled boxes of 64 dims x 128 slots).
+//   warp 1      TMEM owner and MMA issuer: S = Q K^T (A, B from shared memory) and
+//               O += P V (P from TMEM, V from shared memory), fp32 accumulators in TMEM.
+//   warps 4-7   softmax of tile A, one query row per thread: S row from TMEM, online
+//               max / exp2 / sum, P written back to TMEM over S, O rescaled in TMEM
+//               when the row max grows by more than 2^8, final O / l to global.
+//   warps 8-11  the same for tile B.
+// TMEM columns: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512); P_X occupies the
+// first 64 columns of S_X as packed 16-bit pairs.
+//
+// MMA order per K/V tile j (one issuing thread): PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
+// The commit that signals "S_A(j+1) ready" also covers PV_A(j), so when the softmax
+// warps see S_A(j+1) the O_A accumulator is stable and may be rescaled.
+//
+// Every mbarrier wait is bounded (0.5 s of %globaltimer); on expiry the kernel records
+// KVC_DEV_TIMEOUT, drains its own TMA loads and MMAs, frees TMEM and returns, and CTAs
+// that start after the error word carries KVC_DEV_TIMEOUT return at once.
 #include "kvc_internal.h"
 
-bool kvc_tc_supported(const kvc_config&) { return false; }
-bool kvc_tc_make_kv_maps(kvc_cache*) { return false; }
-cudaError_t kvc_launch_attn_tc(kvc_cache*, const void*, void*, int, bool, cudaStream_t) {
-  return cudaErrorNotSupported;
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBM = 128;            // query rows per tile
+constexpr int kBN = 128;            // slots per K/V tile
+constexpr int kStages = 2;
+constexpr int kThreads = 384;
+constexpr uint32_t kBoxBytes = 64 * 2 * 128;         // 64 dims x 128 rows, 16-bit
+constexpr uint32_t kTileBytes = 2 * kBoxBytes;       // 128 dims
+constexpr uint64_t kTimeoutNs = 500000000ull;   // 0.5 s; a healthy wait is microseconds
+constexpr float kRescaleThreshold = 8.0f;            // log2 units
+
+struct Smem {
+  // 1024-byte aligned tiles (128B swizzle atoms)
+  uint8_t q[2][kTileBytes];
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  uint64_t q_full;
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_ready[2], o_done[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// ---- PTX wrappers ----------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity.  Returns false when the CTA is
+// aborting (another role gave up) or when this wait ran out of time (then it starts
+// the abort itself).  `honour_abort` = false is used while draining.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0) {
+      if (honour_abort && *abort) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst, int c0, int c1, int c2,
+                                            int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle, sm_100 descriptor version.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, A/B 16-bit (fmt 0 fp16, 1 bf16),
+// A K-major, B K-major or MN-major, M = 128, N = 128.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t fmt, uint32_t b_mn_major) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | (b_mn_major << 16) | ((uint32_t)(kBN >> 3) << 17) |
+         ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+#define KVC_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                  "=r"(r[i + 6]), "=r"(r[i + 7])
+#define KVC_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), \
+                  "r"(r[i + 7])
+
+// 32 TMEM lanes (one per thread of the warp) x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : KVC_R8(0), KVC_R8(8), KVC_R8(16), KVC_R8(24)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      KVC_W8(0), KVC_W8(8), KVC_W8(16), KVC_W8(24)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Ties 32 registers filled by tmem_ld32 to the preceding wait, so that no use of them
+// is scheduled before the asynchronous load has completed.
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+  asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+               "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+               "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+               "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      KVC_W8(0), KVC_W8(8)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool kBf16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  uint32_t r;
+  if constexpr (kBf16)
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct TcParams {
+  kvc_geom g;
+  int n_q;
+  int causal;
+  float scale_log2;
+};
+
+// ---- the kernel --------------------------------------------------------------
+template <bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+          const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, int32_t* __restrict__ meta, TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int row_a = blockIdx.x * 2 * kBM;
+  const kvc_geom& g = p.g;
+  const int kvh = h / (g.H / g.Hkv);
+
+  // a CTA that starts after another one gave up on a wait returns at once (one read,
+  // shared, so that every thread takes the same branch)
+  if (threadIdx.x == 0)
+    sm.abort = (*reinterpret_cast<volatile int32_t*>(meta + KVC_META_ERR) & KVC_DEV_TIMEOUT) ? 1 : 0;
+  __syncthreads();
+  if (sm.abort) return;
+  int row0 = 0, len = 0;
+  if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;  // same outcome in every thread
+  const int qpos0 = len - p.n_q;                       // absolute position of query 0 (causal)
+  int kv_end = len;
+  if (p.causal) {
+    const int last_row = min(row_a + 2 * kBM, p.n_q) - 1;
+    kv_end = max(1, min(len, qpos0 + last_row + 1));
+  }
+  const int n_tiles = (kv_end + kBN - 1) / kBN;
+  volatile int* abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_ready[t], kBM);
+      mbar_init(&sm.o_done[t], 1);
+    }
+    mbar_init(&sm.drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int kv_batch = g.layout == KVC_PACKED ? 0 : b;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      mbar_expect_tx(&sm.q_full, 2 * kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(&tm_q, &sm.q_full, sm.q[t] + half * kBoxBytes, half * 64, h, row_a + t * kBM, b);
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kStages, u = j / kStages;
+        if (j >= kStages && !mbar_wait(&sm.k_empty[s], (u - 1) & 1, abort)) break;
+        mbar_expect_tx(&sm.k_full[s], kTileBytes);
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(&tm_k, &sm.k_full[s], sm.k[s] + half * kBoxBytes, half * 64, kvh, row0 + j * kBN, kv_batch);
+        k_issued = j + 1;
+        if (j >= kStages && !mbar_wait(&sm.v_empty[s], (u - 1) & 1, abort)) break;
+        mbar_expect_tx(&sm.v_full[s], kTileBytes);
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(&tm_v, &sm.v_full[s], sm.v[s] + half * kBoxBytes, half * 64, kvh, row0 + j * kBN, kv_batch);
+        v_issued = j + 1;
+      }
+      if (*abort) {
+        // drain: every load this thread issued lands before the CTA's shared memory is released
+        mbar_wait(&sm.q_full, 0, abort, false);
+        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
+          mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, abort, false);
+        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
+          mbar_wait(&sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (lane 0) + V tail zeroing (whole warp) ----------------
+    constexpr uint32_t kIdQK = idesc_f16(kBf16 ? 1u : 0u, 0);
+    constexpr uint32_t kIdPV = idesc_f16(kBf16 ? 1u : 0u, 1);
+    const uint32_t s_col[2] = {0u, 128u}, o_col[2] = {256u, 384u};
+    auto issue_qk = [&](int t, int s) {
+      const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[s]);
+#pragma unroll
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+        mma_ss(tmem + s_col[t], sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdQK, kk > 0);
+      }
+    };
+    auto issue_pv = [&](int t, int s, int j) {
+      const uint32_t va = smem_u32(sm.v[s]);
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
+               (j > 0 || kk > 0) ? 1u : 0u);
+    };
+    bool ok = mbar_wait(&sm.q_full, 0, abort) && mbar_wait(&sm.k_full[0], 0, abort);
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok) {
+      tc_fence_after();
+      if (lane == 0) {
+        issue_qk(0, 0);
+        mma_commit(&sm.s_full[0]);
+        issue_qk(1, 0);
+        mma_commit(&sm.s_full[1]);
+        mma_commit(&sm.k_empty[0]);
+      }
+      __syncwarp();
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int s = j % kStages, u = j / kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
+      if (!ok) break;
+      const int rem = kv_end - j * kBN;
+      if (rem < kBN) {
+        // slots past the valid range may hold anything (NaN included): zero those V rows
+        // so that P = 0 there contributes exactly nothing
+        for (int e = lane; e < (kBN - rem) * 2 * 8; e += 32) {
+          const int r = rem + e / 16, half = (e / 8) & 1, c = e & 7;
+          *reinterpret_cast<uint4*>(sm.v[s] + half * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async();
+        __syncwarp();
+      }
+      const bool more = j + 1 < n_tiles;
+      const int s1 = (j + 1) % kStages, u1 = (j + 1) / kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[0], j & 1, abort));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) issue_pv(0, s, j);
+      if (more) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s1], u1 & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          issue_qk(0, s1);
+          mma_commit(&sm.s_full[0]);
+        }
+      } else if (lane == 0) {
+        mma_commit(&sm.o_done[0]);
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[1], j & 1, abort));
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        issue_pv(1, s, j);
+        mma_commit(&sm.v_empty[s]);
+        if (more) {
+          issue_qk(1, s1);
+          mma_commit(&sm.s_full[1]);
+          mma_commit(&sm.k_empty[s1]);
+        } else {
+          mma_commit(&sm.o_done[1]);
+        }
+      }
+      __syncwarp();
+    }
+    if (*abort && lane == 0) {
+      // drain: all MMAs issued by this thread complete before TMEM is released
+      mma_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0, abort, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- softmax (one query row per thread) ----------------
+    const int t = (warp - 4) >> 2;          // query tile A or B
+    const int quad = warp & 3;              // TMEM lane quadrant of this warp
+    const int r = quad * 32 + lane;         // row within the tile
+    const int row = row_a + t * kBM + r;    // query row within the chunk
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+    const uint32_t s_addr = lane_addr + (t ? 128u : 0u);
+    const uint32_t o_addr = lane_addr + (t ? 384u : 256u);
+    const float c = p.scale_log2;
+    const int qpos = qpos0 + row;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, abort));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[128];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_addr + q4 * 32, sr + q4 * 32);
+      tmem_ld_wait();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr + q4 * 32);
+      int valid = kv_end - j * kBN;                          // columns < valid are slots in range
+      if (p.causal) valid = min(valid, qpos - j * kBN + 1);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 128; ++i) {
+        const float x = __uint_as_float(sr[i]);
+        mx = i < valid ? fmaxf(mx, x) : mx;
+      }
+      const float m_tile = mx * c;
+      bool rescale = m_tile > m_ref + kRescaleThreshold;
+      const float m_new = rescale ? m_tile : m_ref;
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      if (__any_sync(0xffffffffu, rescale) && j > 0) {
+        const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t orow[32];
+          tmem_ld32(o_addr + q4 * 32, orow);
+          tmem_ld_wait();
+          reg_fence32(orow);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+          tmem_st32(o_addr + q4 * 32, orow);
+        }
+        tmem_st_wait();
+        l *= alpha;
+      }
+      m_ref = m_new;
+      float sum = 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c0 = q4 * 32 + 2 * i;
+          const float x0 = c0 < valid ? ex2(fmaf(__uint_as_float(sr[c0]), c, -m_use)) : 0.f;
+          const float x1 = c0 + 1 < valid ? ex2(fmaf(__uint_as_float(sr[c0 + 1]), c, -m_use)) : 0.f;
+          sum += x0 + x1;
+          pk[i] = pack2<kBf16>(x0, x1);
+        }
+        tmem_st16(s_addr + q4 * 16, pk);
+      }
+      l += sum;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&sm.p_ready[t]);
+    }
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], 0, abort));
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const bool store = row < p.n_q;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(out) + (((int64_t)b * p.n_q + row) * g.H + h) * kD;
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t orow[32];
+        tmem_ld32(o_addr + q4 * 32, orow);
+        tmem_ld_wait();
+        reg_fence32(orow);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2<kBf16>(__uint_as_float(orow[2 * i]) * inv, __uint_as_float(orow[2 * i + 1]) * inv);
+        if (store) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && sm.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
+}
+
+// ---- host side ----------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 4-D map over a [d3][d2][d1][128] tensor of 16-bit elements, boxes of 64 x 1 x 128 x 1.
+bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t d1, uint64_t d2, uint64_t d3) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, d1, d2, d3};
+  const cuuint64_t strides[3] = {kD * 2ull, d1 * kD * 2ull, d2 * d1 * kD * 2ull};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return enc(m, t, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t smem_bytes() { return sizeof(Smem) + 1024; }
+
+}  // namespace
+
+bool kvc_tc_supported(const kvc_config& cfg) {
+  return (cfg.dtype == KVC_BF16 || cfg.dtype == KVC_F16) && cfg.head_dim == kD;
+}
+
+bool kvc_tc_make_kv_maps(kvc_cache* c) {
+  const kvc_config& g = c->cfg;
+  const uint64_t rows = (uint64_t)c->cap;
+  const uint64_t batches = g.layout == KVC_PACKED ? 1 : (uint64_t)g.batch;
+  if (!make_map(&c->tm_k, g.dtype, c->k, g.kv_heads, rows, batches)) return false;
+  if (!make_map(&c->tm_v, g.dtype, c->v, g.kv_heads, rows, batches)) return false;
+  const size_t smem = smem_bytes();
+  if (cudaFuncSetAttribute(k_attn_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return false;
+  if (cudaFuncSetAttribute(k_attn_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return false;
+  return true;
+}
+
+cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal, cudaStream_t s) {
+  const kvc_config& cfg = c->cfg;
+  CUtensorMap tm_q;
+  if (!make_map(&tm_q, cfg.dtype, q, cfg.heads, (uint64_t)n_q, cfg.batch)) return cudaErrorInvalidValue;
+  TcParams p;
+  p.g = kvc_geom{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
+  p.n_q = n_q;
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = c->scale * 1.4426950408889634f;
+  dim3 grid((n_q + 2 * kBM - 1) / (2 * kBM), cfg.heads, cfg.batch);
+  if (cfg.dtype == KVC_BF16)
+    k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, out, c->meta, p);
+  else
+    k_attn_tc<false><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, out, c->meta, p);
+  return cudaGetLastError();
 }

@@ -140,7 +140,8 @@ int kvc_advance(kvc_cache* c, int32_t row, int32_t n_tokens, void* stream) {
 
 int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, const int32_t* d_slots, void* stream) {
   if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;
-  if (n_tokens > c->cap) return KVC_ERR_RANGE;
+  // a packed write reads a padded source: rows past each row's length are skipped
+  if (n_tokens > c->cap && c->cfg.layout != KVC_PACKED) return KVC_ERR_RANGE;
   if (d_slots != nullptr) {
     if (c->cfg.layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;
     if (((uintptr_t)d_slots & 3u) != 0) return KVC_ERR_ARG;

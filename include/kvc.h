@@ -139,11 +139,13 @@ int kvc_advance(kvc_cache* c, int32_t row, int32_t n_tokens, void* stream);
  *  d_slots == NULL: row b's token i goes to its reserved chunk (first slot from the
  *    meta block, so a replayed graph writes the slot the device holds [RING]); for
  *    PACKED to cu_seqlens[b] + i for i < len_b (the pack of [VAR]), tokens past
- *    len_b are ignored.
+ *    len_b are ignored (so n_tokens may exceed a row's length, or the capacity).
  *  d_slots != NULL (device int32[n_tokens]): token i of every row goes to slot
  *    d_slots[i] — one index shared by all rows on the same timeline [IDX item 1].
  *    Not for PACKED.  Entries outside [0, cap) set KVC_DEV_BAD_SLOT and are skipped.
- * Bytes are copied unchanged (bit-exact). */
+ * Bytes are copied unchanged (bit-exact).
+ * Errors: KVC_ERR_RANGE when n_tokens exceeds the per-row slot count (not PACKED);
+ * KVC_ERR_ARG for a circular write whose n_tokens differs from `chunk`. */
 int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
               const int32_t* d_slots, void* stream);
 
