@@ -283,7 +283,7 @@ def ours(args):
     stream = torch.cuda.current_stream()
     cache = kvc.KVCache(w.batch, w.heads, w.kv_heads, w.head_dim, dtype, w.layout, sink=w.sink, window=w.window,
                         chunk=w.chunk)
-    inputs = make_inputs(w, "cuda", pool=w.n_chunks * w.rewrites)
+    inputs = make_inputs(w, "cuda", pool=min(args.pool, w.n_chunks * w.rewrites))
     out = torch.empty_like(inputs[0][0])
     step_flops, per_attend = ring_flops(w)
 
@@ -436,6 +436,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--pool", type=int, default=8,
+                    help="distinct (q, k, v) input sets, reused cyclically over the chunks")
     args = ap.parse_args()
     if args.impl == "reference":
         reference(args)
