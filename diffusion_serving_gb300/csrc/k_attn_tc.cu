@@ -224,6 +224,59 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return r;
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Row max of the 128 scores a thread holds, over columns < valid when kMask (eight
+// independent chains of 3-input maxima so that the reduction is not one long
+// dependency).
+template <bool kMask>
+__device__ __forceinline__ float row_max(const uint32_t* sr, int valid) {
+  float mx[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 128; i += 2) {
+    float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
+    if (kMask) {
+      x0 = i < valid ? x0 : -INFINITY;
+      x1 = i + 1 < valid ? x1 : -INFINITY;
+    }
+    mx[(i >> 1) & 7] = fmax3(mx[(i >> 1) & 7], x0, x1);
+  }
+  return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+}
+
+// p = 2^(s * c - m) for the 128 columns (0 past `valid` when kMask), packed as 16-bit
+// pairs over the first 64 TMEM columns of the row's S; returns the row sum of p.
+// Pairs of columns go through the packed fp32x2 FMA / add.
+template <bool kBf16, bool kMask>
+__device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, float c, float m_use, uint32_t s_addr) {
+  const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
+  float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c0 = q4 * 32 + 2 * i;
+      const float2 t = __ffma2_rn(make_float2(__uint_as_float(sr[c0]), __uint_as_float(sr[c0 + 1])), c2, nm2);
+      float x0 = ex2(t.x), x1 = ex2(t.y);
+      if (kMask) {
+        x0 = c0 < valid ? x0 : 0.f;
+        x1 = c0 + 1 < valid ? x1 : 0.f;
+      }
+      sum[i & 1] = __fadd2_rn(sum[i & 1], make_float2(x0, x1));
+      pk[i] = pack2<kBf16>(x0, x1);
+    }
+    tmem_st16(s_addr + q4 * 16, pk);
+  }
+  return (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
+}
+
 struct TcParams {
   kvc_geom g;
   int n_q;
@@ -429,12 +482,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr + q4 * 32);
       int valid = kv_end - j * kBN;                          // columns < valid are slots in range
       if (p.causal) valid = min(valid, qpos - j * kBN + 1);
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const float x = __uint_as_float(sr[i]);
-        mx = i < valid ? fmaxf(mx, x) : mx;
-      }
+      const bool full = !p.causal && kv_end - j * kBN >= kBN;    // uniform: no column masked
+      const float mx = full ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
       const float m_tile = mx * c;
       bool rescale = m_tile > m_ref + kRescaleThreshold;
       const float m_new = rescale ? m_tile : m_ref;
@@ -448,28 +497,20 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           tmem_ld_wait();
           reg_fence32(orow);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) orow[i] = __float_as_uint(__uint_as_float(orow[i]) * alpha);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[i]), __uint_as_float(orow[i + 1])),
+                                        make_float2(alpha, alpha));
+            orow[i] = __float_as_uint(y.x);
+            orow[i + 1] = __float_as_uint(y.y);
+          }
           tmem_st32(o_addr + q4 * 32, orow);
         }
         tmem_st_wait();
         l *= alpha;
       }
       m_ref = m_new;
-      float sum = 0.f;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c0 = q4 * 32 + 2 * i;
-          const float x0 = c0 < valid ? ex2(fmaf(__uint_as_float(sr[c0]), c, -m_use)) : 0.f;
-          const float x1 = c0 + 1 < valid ? ex2(fmaf(__uint_as_float(sr[c0 + 1]), c, -m_use)) : 0.f;
-          sum += x0 + x1;
-          pk[i] = pack2<kBf16>(x0, x1);
-        }
-        tmem_st16(s_addr + q4 * 16, pk);
-      }
-      l += sum;
+      l += full ? exp_pack_store<kBf16, false>(sr, valid, c, m_use, s_addr)
+                : exp_pack_store<kBf16, true>(sr, valid, c, m_use, s_addr);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&sm.p_ready[t]);
@@ -488,8 +529,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         reg_fence32(orow);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2<kBf16>(__uint_as_float(orow[2 * i]) * inv, __uint_as_float(orow[2 * i + 1]) * inv);
+        for (int i = 0; i < 16; ++i) {
+          const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[2 * i]), __uint_as_float(orow[2 * i + 1])),
+                                      make_float2(inv, inv));
+          pk[i] = pack2<kBf16>(y.x, y.y);
+        }
         if (store) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
 #pragma unroll

@@ -6,11 +6,13 @@
 // of their kv head's K and V (the repeat_interleave expansion of "Problem" is never
 // materialised).  The query is the newest token, so no mask applies.
 //
-// Grid (splits, Hkv, B).  Each block takes an equal share of the row's kv_len slots
-// (the share is computed on the device from kv_len, so the grid depends only on the
-// capacity and a captured graph replays at any length), computes its G score rows
-// into shared memory, their max and exp2 sums, then P.V, and writes an unnormalised
-// partial (O_s, m_s, l_s) to the workspace.  The last block of each (b, kv head) to
+// Grid (splits, Hkv, B).  Each block takes an equal share (at least kMinShare slots)
+// of the row's kv_len slots; the share is computed on the device from kv_len, so the
+// grid depends only on the shape and a captured graph replays at any length.
+// Inside a block every warp streams its slots once, K and V of several slots in
+// flight per lane, keeping an online softmax (running max m, sum l, accumulator) per
+// q head; the warps' states merge in shared memory into one unnormalised partial
+// (O_s, m_s, l_s) written to the workspace.  The last block of each (b, kv head) to
 // finish (a ticket counter in the workspace, left at zero for the next call) merges
 // the partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 //
@@ -25,8 +27,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kTpsMax = 2048;   // most slots one block handles
-constexpr int kUnroll = 4;      // slot groups with loads in flight per lane
+constexpr int kMinShare = 64;    // fewest slots a block takes (short prefixes use few splits)
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f, const __half*) {
   const __half2* h = reinterpret_cast<const __half2*>(&u);
@@ -49,16 +50,24 @@ __device__ __forceinline__ void unpack8(const uint4& u, float* f, const __nv_bfl
 __device__ __forceinline__ void store_out(__half* p, float x) { *p = __float2half_rn(x); }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
 k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst, const T* __restrict__ vst,
          int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2) {
-  constexpr int EPL = D / 8;      // dims per lane
-  constexpr int VPL = EPL / 8;    // 16-byte vectors per lane
-  extern __shared__ float smem[];
-  float* sc = smem;                               // [G][kTpsMax] scores, then probabilities
-  float* red = smem + G * kTpsMax;                // [kWarps][G][D] partial outputs
-  __shared__ float s_m[G], s_l[G];
+  constexpr int EPL = D / 8;                     // dims per lane
+  constexpr int VPL = EPL / 8;                   // 16-byte vectors per lane
+  constexpr int U = (G * EPL > 64) ? 1 : 4;      // slot groups in flight per lane (register budget)
+  constexpr int kStep = kWarps * 4;              // slots between a warp's consecutive groups
+  __shared__ float s_acc[kWarps][G][D];
+  __shared__ float s_ml[kWarps][G][2];
+  __shared__ float s_red[kWarps];
+  __shared__ float s_merge_w[KVC_DECODE_MAX_SPLITS];
   __shared__ int s_last;
 
   const int split = blockIdx.x, nsplit = gridDim.x;
@@ -70,11 +79,11 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
   int row0 = 0, len = 0;
   if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;
 
-  int tps = (len + nsplit - 1) / nsplit;
-  tps = (tps + 15) & ~15;
-  const int t0 = split * tps;
-  const int t1 = min(len, t0 + tps);
-  const int nt = max(0, t1 - t0);
+  int share = (len + nsplit - 1) / nsplit;
+  share = max(share, kMinShare);
+  share = (share + 15) & ~15;
+  const int t0 = split * share;
+  const int nt = max(0, min(len, t0 + share) - t0);
 
   // query slice for this lane's dims, G heads, pre-scaled into the exp2 domain
   float qv[G][EPL];
@@ -83,7 +92,7 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
     const T* qp = q + ((int64_t)b * g.H + kvh * G + gg) * D + sub * EPL;
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
-      uint4 u = *reinterpret_cast<const uint4*>(qp + 8 * v);
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(qp + 8 * v));
       unpack8(u, &qv[gg][8 * v], (const T*)nullptr);
     }
 #pragma unroll
@@ -94,26 +103,39 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
   const T* kbase = kst + kvc_kv_offset(g, b, row0, t0, kvh) + sub * EPL;
   const T* vbase = vst + kvc_kv_offset(g, b, row0, t0, kvh) + sub * EPL;
 
-  // ---- scores ---------------------------------------------------------------
-  // loop bounds are uniform per warp (the shuffles below need every lane)
-  for (int tw = warp * 4; tw < nt; tw += kWarps * 4 * kUnroll) {
-    const int tb = tw + grp;
-    uint4 kr[kUnroll][VPL];
+  float m[G], l[G], acc[G][EPL];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = tb + u * kWarps * 4;
+  for (int gg = 0; gg < G; ++gg) {
+    m[gg] = -INFINITY;
+    l[gg] = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[gg][e] = 0.f;
+  }
+
+  // loop bounds are uniform per warp (the shuffles below need every lane)
+  for (int tw = warp * 4; tw < nt; tw += kStep * U) {
+    uint4 kr[U][VPL], vr[U][VPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int t = tw + grp + u * kStep;
       if (t < nt) {
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) kr[u][v] = __ldg(reinterpret_cast<const uint4*>(kbase + t * row_step) + v);
+        for (int v = 0; v < VPL; ++v) {
+          kr[u][v] = __ldcs(reinterpret_cast<const uint4*>(kbase + t * row_step) + v);
+          vr[u][v] = __ldcs(reinterpret_cast<const uint4*>(vbase + t * row_step) + v);
+        }
+      } else {
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) kr[u][v] = vr[u][v] = make_uint4(0, 0, 0, 0);
       }
     }
+    float s[U][G];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = tb + u * kWarps * 4;
+    for (int u = 0; u < U; ++u) {
       float kf[EPL];
 #pragma unroll
       for (int v = 0; v < VPL; ++v) unpack8(kr[u][v], &kf[8 * v], (const T*)nullptr);
-      float s[G];
+      const bool valid = tw + grp + u * kStep < nt;
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
         float a = 0.f;
@@ -122,74 +144,41 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
         a += __shfl_xor_sync(0xffffffffu, a, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);
         a += __shfl_xor_sync(0xffffffffu, a, 4);
-        s[gg] = a;
-      }
-      if (t < nt) {
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg)
-          if (sub == gg % 8) sc[gg * kTpsMax + t] = s[gg];
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- softmax statistics per head -----------------------------------------
-  for (int gg = warp; gg < G; gg += kWarps) {
-    float mx = -INFINITY;
-    for (int t = lane; t < nt; t += 32) mx = fmaxf(mx, sc[gg * kTpsMax + t]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float sum = 0.f;
-    for (int t = lane; t < nt; t += 32) {
-      const float p = exp2f(sc[gg * kTpsMax + t] - mx);
-      sc[gg * kTpsMax + t] = p;
-      sum += p;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    if (lane == 0) {
-      s_m[gg] = mx;
-      s_l[gg] = sum;
-    }
-  }
-  __syncthreads();
-
-  // ---- P.V ------------------------------------------------------------------
-  float acc[G][EPL];
-#pragma unroll
-  for (int gg = 0; gg < G; ++gg)
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[gg][e] = 0.f;
-  for (int tw = warp * 4; tw < nt; tw += kWarps * 4 * kUnroll) {
-    const int tb = tw + grp;
-    uint4 vr[kUnroll][VPL];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = tb + u * kWarps * 4;
-      if (t < nt) {
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) vr[u][v] = __ldg(reinterpret_cast<const uint4*>(vbase + t * row_step) + v);
+        s[u][gg] = valid ? a : -INFINITY;
       }
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int t = tb + u * kWarps * 4;
-      if (t < nt) {
+    for (int gg = 0; gg < G; ++gg) {
+      float mx = s[0][gg];
+#pragma unroll
+      for (int u = 1; u < U; ++u) mx = fmaxf(mx, s[u][gg]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      // finite: slot tw (group 0, u = 0) is valid on every pass of this loop
+      const float mnew = fmaxf(m[gg], mx);
+      const float alpha = ex2(m[gg] - mnew);
+      m[gg] = mnew;
+      l[gg] *= alpha;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[gg][e] *= alpha;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float p = ex2(s[u][gg] - mnew);
+        l[gg] += p;
         float vf[EPL];
 #pragma unroll
         for (int v = 0; v < VPL; ++v) unpack8(vr[u][v], &vf[8 * v], (const T*)nullptr);
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          const float p = sc[gg * kTpsMax + t];
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) acc[gg][e] = fmaf(p, vf[e], acc[gg][e]);
-        }
+        for (int e = 0; e < EPL; ++e) acc[gg][e] = fmaf(p, vf[e], acc[gg][e]);
       }
     }
   }
-  // reduce the warp's 4 slot groups, then the warps through shared memory
+  // Sum the warp's 4 slot groups (they share m).  Every lane of a group added the
+  // same p values to l, so after the sum any lane holds the warp's total.
 #pragma unroll
-  for (int gg = 0; gg < G; ++gg)
+  for (int gg = 0; gg < G; ++gg) {
+    l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 8);
+    l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 16);
 #pragma unroll
     for (int e = 0; e < EPL; ++e) {
       float a = acc[gg][e];
@@ -197,28 +186,49 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
       a += __shfl_xor_sync(0xffffffffu, a, 16);
       acc[gg][e] = a;
     }
+  }
   if (grp == 0) {
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg)
+    for (int gg = 0; gg < G; ++gg) {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) red[(warp * G + gg) * D + sub * EPL + e] = acc[gg][e];
+      for (int e = 0; e < EPL; ++e) s_acc[warp][gg][sub * EPL + e] = acc[gg][e];
+      if (sub == 0) {
+        s_ml[warp][gg][0] = m[gg];
+        s_ml[warp][gg][1] = l[gg];
+      }
+    }
   }
   __syncthreads();
 
+  // ---- this block's partial: merge the warps ---------------------------------
   const int pairs = g.B * g.Hkv;
   const int pair = b * g.Hkv + kvh;
   float* ws_o = ws;                                              // [pairs][nsplit][G][D]
   float* ws_ml = ws + (int64_t)pairs * nsplit * G * D;           // [pairs][nsplit][G][2]
   int* tickets = reinterpret_cast<int*>(ws_ml + (int64_t)pairs * nsplit * G * 2);  // [pairs]
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int gg = e / D, d = e - gg * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][gg][0]);
     float a = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) a += red[w * G * D + e];
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = s_ml[w][gg][0];
+      if (mw != -INFINITY) a = fmaf(ex2(mw - M), s_acc[w][gg][d], a);
+    }
     ws_o[((int64_t)pair * nsplit + split) * G * D + e] = a;
   }
   if (threadIdx.x < G) {
-    ws_ml[(((int64_t)pair * nsplit + split) * G + threadIdx.x) * 2 + 0] = s_m[threadIdx.x];
-    ws_ml[(((int64_t)pair * nsplit + split) * G + threadIdx.x) * 2 + 1] = s_l[threadIdx.x];
+    const int gg = threadIdx.x;
+    float M = -INFINITY, L = 0.f;
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][gg][0]);
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = s_ml[w][gg][0];
+      if (mw != -INFINITY) L = fmaf(ex2(mw - M), s_ml[w][gg][1], L);
+    }
+    ws_ml[(((int64_t)pair * nsplit + split) * G + gg) * 2 + 0] = M;
+    ws_ml[(((int64_t)pair * nsplit + split) * G + gg) * 2 + 1] = L;
   }
   __threadfence();
   __syncthreads();
@@ -228,49 +238,73 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
   __threadfence();
 
   // ---- merge the splits (last block of this (b, kv head)) -------------------
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int gg = e / D, d = e - gg * D;
+  const int used = min(nsplit, (len + share - 1) / share);       // later splits are empty
+  for (int gg = 0; gg < G; ++gg) {
     float M = -INFINITY;
-    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2));
-    float L = 0.f, o = 0.f;
-    for (int s = 0; s < nsplit; ++s) {
+    for (int s = threadIdx.x; s < used; s += blockDim.x)
+      M = fmaxf(M, __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) s_red[warp] = M;
+    __syncthreads();
+    M = s_red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_red[w]);
+    __syncthreads();
+    float L = 0.f;
+    for (int s = threadIdx.x; s < used; s += blockDim.x) {
       const float ms = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2);
       const float ls = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2 + 1);
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      L = fmaf(w, ls, L);
-      o = fmaf(w, __ldcg(ws_o + ((int64_t)pair * nsplit + s) * G * D + e), o);
+      const float wgt = ms == -INFINITY ? 0.f : ex2(ms - M);
+      s_merge_w[s] = wgt;
+      L = fmaf(wgt, ls, L);
     }
-    store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, o / L);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) s_red[warp] = L;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += s_red[w];
+    const float inv = 1.f / tot;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+      float o0 = 0.f, o1 = 0.f;
+      int s = 0;
+      for (; s + 1 < used; s += 2) {
+        o0 = fmaf(s_merge_w[s], __ldcg(ws_o + (((int64_t)pair * nsplit + s) * G + gg) * D + d), o0);
+        o1 = fmaf(s_merge_w[s + 1], __ldcg(ws_o + (((int64_t)pair * nsplit + s + 1) * G + gg) * D + d), o1);
+      }
+      if (s < used) o0 = fmaf(s_merge_w[s], __ldcg(ws_o + (((int64_t)pair * nsplit + s) * G + gg) * D + d), o0);
+      store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, (o0 + o1) * inv);
+    }
+    __syncthreads();
   }
   if (threadIdx.x == 0) tickets[pair] = 0;
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare_only) {
+cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
-  const size_t smem = (size_t)G * kTpsMax * 4 + (size_t)kWarps * G * D * 4;
-  auto fn = k_decode<T, D, G>;
-  if (prepare_only) return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
-  fn<<<grid, kThreads, smem, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta, (float*)c->ws, g,
-                                  c->scale * 1.4426950408889634f);
+  k_decode<T, D, G><<<grid, kThreads, 0, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta,
+                                              (float*)c->ws, g, c->scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-cudaError_t launch_d(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prep) {
+cudaError_t launch_d(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
   switch (c->cfg.heads / c->cfg.kv_heads) {
-    case 1: return launch_dg<T, D, 1>(c, q, out, s, prep);
-    case 2: return launch_dg<T, D, 2>(c, q, out, s, prep);
-    case 4: return launch_dg<T, D, 4>(c, q, out, s, prep);
-    default: return launch_dg<T, D, 8>(c, q, out, s, prep);
+    case 1: return launch_dg<T, D, 1>(c, q, out, s);
+    case 2: return launch_dg<T, D, 2>(c, q, out, s);
+    case 4: return launch_dg<T, D, 4>(c, q, out, s);
+    default: return launch_dg<T, D, 8>(c, q, out, s);
   }
 }
 
 template <typename T>
-cudaError_t launch_t(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prep) {
-  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, s, prep) : launch_d<T, 128>(c, q, out, s, prep);
+cudaError_t launch_t(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
+  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, s) : launch_d<T, 128>(c, q, out, s);
 }
 
 }  // namespace
@@ -288,12 +322,5 @@ size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits) {
 }
 
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
-  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, s, false) : launch_t<__nv_bfloat16>(c, q, out, s, false);
-}
-
-// Opt the config's decode kernel into its dynamic shared memory (done at create time,
-// so no attribute call happens while a stream is being captured).
-cudaError_t kvc_prepare_decode(kvc_cache* c) {
-  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, nullptr, nullptr, 0, true)
-                                 : launch_t<__nv_bfloat16>(c, nullptr, nullptr, 0, true);
+  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, s) : launch_t<__nv_bfloat16>(c, q, out, s);
 }

@@ -50,8 +50,7 @@ int check_cfg(const kvc_config* cfg, int* cap) {
 int decode_splits(const kvc_config& cfg, int cap) {
   const int pairs = cfg.batch * cfg.kv_heads;
   int n = (kDecodeTargetBlocks + pairs - 1) / pairs;
-  const int need = (cap + 2047) / 2048;
-  if (n < need) n = need;
+  if (n > KVC_DECODE_MAX_SPLITS) n = KVC_DECODE_MAX_SPLITS;
   if (n > cap) n = cap;
   return n < 1 ? 1 : n;
 }
@@ -104,10 +103,6 @@ int kvc_create(const kvc_config* cfg, void* k_store, void* v_store, void* meta, 
   c->dec_splits = kvc_decode_supported(*cfg) ? decode_splits(*cfg, cap) : 0;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess) {
-    delete c;
-    return KVC_ERR_CUDA;
-  }
-  if (c->dec_splits > 0 && kvc_prepare_decode(c) != cudaSuccess) {
     delete c;
     return KVC_ERR_CUDA;
   }

@@ -73,6 +73,9 @@ __device__ __forceinline__ int64_t kvc_kv_offset(const kvc_geom& g, int b, int r
   return (row * g.Hkv + kvh) * (int64_t)g.D;
 }
 
+// Most splits the decode kernel takes per (row, kv head).
+#define KVC_DECODE_MAX_SPLITS 1024
+
 // ---- launchers (each returns a cudaError_t from the launch) ------------------
 cudaError_t kvc_launch_advance(kvc_cache* c, int row, int n, cudaStream_t s);
 cudaError_t kvc_launch_reset(kvc_cache* c, int row, cudaStream_t s);
@@ -82,7 +85,6 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
 cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
                                  cudaStream_t s);
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s);
-cudaError_t kvc_prepare_decode(kvc_cache* c);
 bool kvc_decode_supported(const kvc_config& cfg);
 size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits);
 cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
