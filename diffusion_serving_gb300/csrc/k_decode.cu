@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -323,4 +325,85 @@ size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits) {
 
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
   return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, s) : launch_t<__nv_bfloat16>(c, q, out, s);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode entry point.
+//
+// Some callers cannot allocate device memory at all: code running inside another
+// framework's memory pool, plugins whose host process owns every cudaMalloc, or
+// steps that must not allocate once a graph has been captured.  They still own the
+// K/V stores, the meta block, the query and the output, but have nowhere to put the
+// decode kernel's scratch (per-split partial outputs and the per-(row, kv head)
+// tickets).  kvc_attend_decode_noalloc gives them the same decode kernel with that
+// scratch in a fixed array compiled into this library: kDecodeScratchBytes (4 MiB)
+// of device memory that every GPU which loads the library holds until the process
+// exits.  All calls share it, so calls that overlap on the GPU (different streams,
+// or different host threads without ordering) race on it; calls on one stream are
+// ordered and safe.  It keeps the last call's contents; the tickets, which must
+// start at zero, are cleared by every call.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kDecodeScratchBytes = 4u << 20;
+constexpr int kMaxDevices = 64;
+
+__device__ __align__(256) unsigned char g_decode_scratch[kDecodeScratchBytes];
+
+// Device address of g_decode_scratch, looked up once per device with that device
+// current.  In host code the array's name is only a stand-in for the symbol, never
+// a pointer a kernel may be given.
+void* g_scratch_ptr[kMaxDevices];
+std::mutex g_scratch_mu;
+
+cudaError_t scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" int kvc_attend_decode_noalloc(const kvc_config* cfg, const void* k_store, const void* v_store,
+                                         int32_t* meta, const void* q, void* out, void* stream) {
+  int cap = 0;
+  const int rc = kvc_internal_check_config(cfg, &cap);
+  if (rc != KVC_OK) return rc;
+  if (!kvc_decode_supported(*cfg)) return KVC_ERR_UNSUPPORTED;
+  const uintptr_t mis = (uintptr_t)k_store | (uintptr_t)v_store | (uintptr_t)meta | (uintptr_t)q | (uintptr_t)out;
+  if (!k_store || !v_store || !meta || !q || !out || (mis & 15u)) return KVC_ERR_ARG;
+  const int splits = kvc_internal_decode_splits(*cfg, cap);
+  const size_t need = kvc_decode_workspace_bytes(*cfg, splits);
+  if (need > kDecodeScratchBytes) return KVC_ERR_RANGE;   // too many (row, kv head) pairs for the array
+  void* scratch = nullptr;
+  if (scratch_for_current_device(&scratch) != cudaSuccess) return KVC_ERR_CUDA;
+
+  // the same kernel as kvc_attend's decode path, on a handle that lives on this stack
+  kvc_cache c{};
+  c.cfg = *cfg;
+  c.cap = cap;
+  c.eb = 2;
+  c.scale = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0f / sqrtf((float)cfg->head_dim);
+  c.k = const_cast<void*>(k_store);
+  c.v = const_cast<void*>(v_store);
+  c.meta = meta;
+  c.ws = scratch;
+  c.dec_splits = splits;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the tickets sit after the partials; an earlier call with another shape may have
+  // left partial data there
+  const size_t pairs = (size_t)cfg->batch * cfg->kv_heads;
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - pairs * 4), 0, pairs * 4, s) != cudaSuccess)
+    return KVC_ERR_CUDA;
+  return kvc_launch_decode(&c, q, out, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }

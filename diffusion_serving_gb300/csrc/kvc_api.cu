@@ -61,6 +61,9 @@ int launched(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
 
 }  // namespace
 
+int kvc_internal_check_config(const kvc_config* cfg, int* cap) { return check_cfg(cfg, cap); }
+int kvc_internal_decode_splits(const kvc_config& cfg, int cap) { return decode_splits(cfg, cap); }
+
 extern "C" {
 
 size_t kvc_meta_bytes(const kvc_config* cfg) {

@@ -86,6 +86,8 @@ cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q
                                  cudaStream_t s);
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s);
 bool kvc_decode_supported(const kvc_config& cfg);
+int kvc_internal_check_config(const kvc_config* cfg, int* cap);
+int kvc_internal_decode_splits(const kvc_config& cfg, int cap);
 size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits);
 cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
                                cudaStream_t s);

@@ -63,6 +63,7 @@ def _load():
         "kvc_get_error": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
         "kvc_destroy": (ctypes.c_int, [P]),
         "kvc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+        "kvc_attend_decode_noalloc": (ctypes.c_int, [cfgp, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -164,6 +165,12 @@ def kvc_destroy(h: int) -> None:
 
 def kvc_strerror(code: int) -> str:
     return _lib.kvc_strerror(code).decode()
+
+
+def kvc_attend_decode_noalloc(cfg: kvc_config, k_store, v_store, meta, q, out, stream=None) -> None:
+    """Decode attention for callers that cannot allocate device memory (see kvc.h)."""
+    _check(_lib.kvc_attend_decode_noalloc(ctypes.byref(cfg), _ptr(k_store), _ptr(v_store), _ptr(meta), _ptr(q),
+                                          _ptr(out), _stream(stream)), "kvc_attend_decode_noalloc")
 
 
 # ---------------------------------------------------------------------------

@@ -187,6 +187,27 @@ int kvc_destroy(kvc_cache* c);
 /* Static string for a return code. */
 const char* kvc_strerror(int code);
 
+/* Decode attention without any device allocation and without a handle.  The pages
+ * have no counterpart: this entry point exists for callers that cannot allocate
+ * device memory themselves, such as code running inside another framework's memory
+ * pool, plugins whose host process owns every allocation, or a serving step that must
+ * not allocate once its graphs are captured.  They cannot provide kvc_create's
+ * workspace, so this call runs the split-KV decode kernel of kvc_attend (n_q == 1)
+ * with its scratch in a fixed 4 MiB array inside libkvc.so, held on every GPU that
+ * loads the library until the process exits.
+ *  cfg: as for kvc_create (F16 / BF16, head_dim 64 or 128, H/Hkv in {1,2,4,8}).
+ *  k_store, v_store, meta: the caller's store and meta block (kv_len or cu_seqlens
+ *    already set, e.g. through a handle's kvc_advance / kvc_set_lengths);
+ *  q: device [B, 1, H, D]; out: device [B, 1, H, D]; all 16-byte aligned.
+ * Returns KVC_ERR_RANGE when the scratch would exceed 4 MiB (too many (row, kv head)
+ * pairs), KVC_ERR_ARG / KVC_ERR_UNSUPPORTED as kvc_create, KVC_ERR_CUDA.  Calls no
+ * cudaMalloc or cudaFree.  The first call on a device looks up the array's device
+ * address (make that call before any stream capture).  Every call shares the array
+ * and clears the part that must start at zero; calls that overlap on the GPU (other
+ * streams, or host threads without ordering) race on it. */
+int kvc_attend_decode_noalloc(const kvc_config* cfg, const void* k_store, const void* v_store,
+                              int32_t* meta, const void* q, void* out, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
