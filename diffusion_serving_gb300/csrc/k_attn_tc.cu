@@ -324,7 +324,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
-      mbar_init(&sm.p_ready[t], kBM);
+      mbar_init(&sm.p_ready[t], kBM / 32);   // one arrival per softmax warp
       mbar_init(&sm.o_done[t], 1);
     }
     mbar_init(&sm.drain, 1);
@@ -513,7 +513,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                 : exp_pack_store<kBf16, true>(sr, valid, c, m_use, s_addr);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&sm.p_ready[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.p_ready[t]);
     }
     ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], 0, abort));
     if (ok) {

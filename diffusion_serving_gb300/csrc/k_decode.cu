@@ -29,7 +29,57 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMinShare = 64;    // fewest slots a block takes (short prefixes use few splits)
+constexpr int kMinShare = 64;       // fewest slots a block takes (short prefixes use few splits)
+constexpr int kChunk = 8;           // slots per pipeline stage of a warp (two groups of 4)
+constexpr int kStages = 4;          // stages per warp: 3 chunks in flight while one is consumed
+constexpr uint64_t kTimeoutNs = 500000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait (0.5 s of %globaltimer); false when it ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 63) == 0 && globaltimer() - t0 > kTimeoutNs) return false;
+  }
+}
+
+// One contiguous global -> shared copy on the bulk-copy (TMA) engine, completion
+// counted in bytes on `bar`.  Addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* f, const __half*) {
   const __half2* h = reinterpret_cast<const __half2*>(&u);
@@ -58,25 +108,35 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+template <int D, typename T>
+__host__ __device__ constexpr size_t stage_bytes() { return (size_t)kChunk * D * sizeof(T) * 2; }   // K and V rows of a chunk
+
+template <int D, typename T>
+__host__ __device__ constexpr size_t dyn_smem_bytes() { return (size_t)kWarps * kStages * stage_bytes<D, T>(); }
+
+// Lane mapping: 8 lanes (sub = 0..7) per slot row, 4 rows per warp instruction (grp).
+// Lane sub holds dims {64 v + 8 sub + i : v < D/64, i < 8}, so that the 8 lanes of a
+// group read 128 contiguous bytes of a row per 16-byte load (conflict-free).
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst, const T* __restrict__ vst,
          int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2) {
-  constexpr int EPL = D / 8;                     // dims per lane
-  constexpr int VPL = EPL / 8;                   // 16-byte vectors per lane
-  constexpr int U = (G * EPL > 64) ? 1 : 4;      // slot groups in flight per lane (register budget)
-  constexpr int kStep = kWarps * 4;              // slots between a warp's consecutive groups
+  constexpr int VPL = D / 64;        // 16-byte vectors per lane per row
+  constexpr int EPL = VPL * 8;       // dims per lane
+  constexpr int ROW = D * (int)sizeof(T);
+  constexpr int SB = (int)stage_bytes<D, T>();
+  extern __shared__ __align__(128) uint8_t dsm[];     // [kWarps][kStages][K rows | V rows]
+  __shared__ uint64_t bars[kWarps][kStages];
   __shared__ float s_acc[kWarps][G][D];
   __shared__ float s_ml[kWarps][G][2];
-  __shared__ float s_red[kWarps];
-  __shared__ float s_merge_w[KVC_DECODE_MAX_SPLITS];
-  __shared__ int s_last;
+  __shared__ float s_inv[G];
+  __shared__ int s_last, s_timeout;
 
   const int split = blockIdx.x, nsplit = gridDim.x;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane & 7;        // dim slice
-  const int grp = lane >> 3;       // slot within the warp's 4
+  const int sub = lane & 7;          // dim slice
+  const int grp = lane >> 3;         // slot within the group of 4
 
   int row0 = 0, len = 0;
   if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;
@@ -87,23 +147,45 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
   const int t0 = split * share;
   const int nt = max(0, min(len, t0 + share) - t0);
 
+  if (threadIdx.x < kWarps * kStages) mbar_init(&bars[0][0] + threadIdx.x, 1);
+  if (threadIdx.x == 0) s_timeout = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+
+  // this warp's chunks: slots [t0 + kChunk (warp + kWarps i), +kChunk) for i = 0, 1, ...
+  const int n_chunks = nt > warp * kChunk ? (nt - warp * kChunk + kWarps * kChunk - 1) / (kWarps * kChunk) : 0;
+  uint8_t* wsm = dsm + (size_t)warp * kStages * SB;
+  const int64_t row_step = (int64_t)g.Hkv * D;         // elements between consecutive slots
+  const T* kbase = kst + kvc_kv_offset(g, b, row0, t0, kvh);
+  const T* vbase = vst + kvc_kv_offset(g, b, row0, t0, kvh);
+  auto issue = [&](int i) {                            // whole warp; lanes 0-15 copy one row each
+    const int st = i % kStages;
+    const int first = (warp + kWarps * i) * kChunk;
+    const int nvalid = min(kChunk, nt - first);
+    if (lane == 0) mbar_expect_tx(&bars[warp][st], (uint32_t)(2 * nvalid * ROW));
+    __syncwarp();
+    const int r = lane & 7;
+    if (lane < 16 && r < nvalid) {
+      const T* src = (lane < 8 ? kbase : vbase) + (int64_t)(first + r) * row_step;
+      bulk_g2s(wsm + st * SB + (lane < 8 ? 0 : kChunk * ROW) + r * ROW, src, ROW, &bars[warp][st]);
+    }
+  };
+  int issued = 0;
+  for (; issued < kStages && issued < n_chunks; ++issued) issue(issued);
+
   // query slice for this lane's dims, G heads, pre-scaled into the exp2 domain
   float qv[G][EPL];
 #pragma unroll
   for (int gg = 0; gg < G; ++gg) {
-    const T* qp = q + ((int64_t)b * g.H + kvh * G + gg) * D + sub * EPL;
+    const T* qp = q + ((int64_t)b * g.H + kvh * G + gg) * D;
 #pragma unroll
     for (int v = 0; v < VPL; ++v) {
-      uint4 u = __ldg(reinterpret_cast<const uint4*>(qp + 8 * v));
+      uint4 u = __ldg(reinterpret_cast<const uint4*>(qp + 64 * v + 8 * sub));
       unpack8(u, &qv[gg][8 * v], (const T*)nullptr);
     }
 #pragma unroll
     for (int e = 0; e < EPL; ++e) qv[gg][e] *= scale_log2;
   }
-
-  const int64_t row_step = (int64_t)g.Hkv * D;   // elements between consecutive slots
-  const T* kbase = kst + kvc_kv_offset(g, b, row0, t0, kvh) + sub * EPL;
-  const T* vbase = vst + kvc_kv_offset(g, b, row0, t0, kvh) + sub * EPL;
 
   float m[G], l[G], acc[G][EPL];
 #pragma unroll
@@ -114,66 +196,86 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
     for (int e = 0; e < EPL; ++e) acc[gg][e] = 0.f;
   }
 
-  // loop bounds are uniform per warp (the shuffles below need every lane)
-  for (int tw = warp * 4; tw < nt; tw += kStep * U) {
-    uint4 kr[U][VPL], vr[U][VPL];
+  bool ok = true;
+  for (int i = 0; i < n_chunks; ++i) {
+    const int st = i % kStages;
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars[warp][st], (i / kStages) & 1));
+    if (!ok) break;
+    const int first = (warp + kWarps * i) * kChunk;
+    const uint8_t* ks = wsm + st * SB;
+    const uint8_t* vs = ks + kChunk * ROW;
+    float sc[2][G];
+    bool valid[2];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int t = tw + grp + u * kStep;
-      if (t < nt) {
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-          kr[u][v] = __ldcs(reinterpret_cast<const uint4*>(kbase + t * row_step) + v);
-          vr[u][v] = __ldcs(reinterpret_cast<const uint4*>(vbase + t * row_step) + v);
-        }
-      } else {
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) kr[u][v] = vr[u][v] = make_uint4(0, 0, 0, 0);
-      }
-    }
-    float s[U][G];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < 2; ++u) {
+      const int r = u * 4 + grp;
+      valid[u] = first + r < nt;
       float kf[EPL];
 #pragma unroll
-      for (int v = 0; v < VPL; ++v) unpack8(kr[u][v], &kf[8 * v], (const T*)nullptr);
-      const bool valid = tw + grp + u * kStep < nt;
+      for (int v = 0; v < VPL; ++v)
+        unpack8(*reinterpret_cast<const uint4*>(ks + r * ROW + v * 128 + sub * 16), &kf[8 * v], (const T*)nullptr);
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
-        float a = 0.f;
+        float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) a = fmaf(qv[gg][e], kf[e], a);
+        for (int e = 0; e < EPL; e += 2)
+          a2 = __ffma2_rn(make_float2(qv[gg][e], qv[gg][e + 1]), make_float2(kf[e], kf[e + 1]), a2);
+        float a = a2.x + a2.y;
         a += __shfl_xor_sync(0xffffffffu, a, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);
         a += __shfl_xor_sync(0xffffffffu, a, 4);
-        s[u][gg] = valid ? a : -INFINITY;
+        sc[u][gg] = valid[u] ? a : -INFINITY;
       }
     }
+    float vf[2][EPL];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int r = u * 4 + grp;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+        unpack8(*reinterpret_cast<const uint4*>(vs + r * ROW + v * 128 + sub * 16), &vf[u][8 * v], (const T*)nullptr);
+    }
+    if (first + kChunk > nt) {                           // the warp's last, partial chunk
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) vf[u][e] = valid[u] ? vf[u][e] : 0.f;   // stale rows past nt
+    }
+    __syncwarp();
+    if (issued < n_chunks) issue(issued++);             // refill this stage (chunk i + kStages) while computing
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
-      float mx = s[0][gg];
-#pragma unroll
-      for (int u = 1; u < U; ++u) mx = fmaxf(mx, s[u][gg]);
+      float mx = fmaxf(sc[0][gg], sc[1][gg]);
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      // finite: slot tw (group 0, u = 0) is valid on every pass of this loop
-      const float mnew = fmaxf(m[gg], mx);
-      const float alpha = ex2(m[gg] - mnew);
-      m[gg] = mnew;
-      l[gg] *= alpha;
+      if (mx > m[gg]) {                                  // warp-uniform: the running max grows
+        const float alpha = ex2(m[gg] - mx);             // 0 on the first chunk (m = -inf)
+        m[gg] = mx;
+        l[gg] *= alpha;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[gg][e] *= alpha;
+        for (int e = 0; e < EPL; e += 2) {
+          const float2 y = __fmul2_rn(make_float2(acc[gg][e], acc[gg][e + 1]), make_float2(alpha, alpha));
+          acc[gg][e] = y.x;
+          acc[gg][e + 1] = y.y;
+        }
+      }
+      const float p0 = ex2(sc[0][gg] - m[gg]), p1 = ex2(sc[1][gg] - m[gg]);
+      l[gg] += p0 + p1;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const float p = ex2(s[u][gg] - mnew);
-        l[gg] += p;
-        float vf[EPL];
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) unpack8(vr[u][v], &vf[8 * v], (const T*)nullptr);
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[gg][e] = fmaf(p, vf[e], acc[gg][e]);
+      for (int e = 0; e < EPL; e += 2) {
+        float2 y = make_float2(acc[gg][e], acc[gg][e + 1]);
+        y = __ffma2_rn(make_float2(p0, p0), make_float2(vf[0][e], vf[0][e + 1]), y);
+        y = __ffma2_rn(make_float2(p1, p1), make_float2(vf[1][e], vf[1][e + 1]), y);
+        acc[gg][e] = y.x;
+        acc[gg][e + 1] = y.y;
       }
     }
+  }
+  if (!ok) {
+    // give up: record it, then let this warp's copies in flight land before the block exits
+    if (lane == 0) s_timeout = 1;
+    for (int c = max(0, issued - kStages); c < issued; ++c)   // newest chunk issued to each stage
+      mbar_wait(&bars[warp][c % kStages], (c / kStages) & 1);
   }
   // Sum the warp's 4 slot groups (they share m).  Every lane of a group added the
   // same p values to l, so after the sum any lane holds the warp's total.
@@ -193,7 +295,7 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) s_acc[warp][gg][sub * EPL + e] = acc[gg][e];
+      for (int e = 0; e < EPL; ++e) s_acc[warp][gg][(e >> 3) * 64 + sub * 8 + (e & 7)] = acc[gg][e];
       if (sub == 0) {
         s_ml[warp][gg][0] = m[gg];
         s_ml[warp][gg][1] = l[gg];
@@ -201,6 +303,7 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0 && s_timeout) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 
   // ---- this block's partial: merge the warps ---------------------------------
   const int pairs = g.B * g.Hkv;
@@ -240,73 +343,95 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
   __threadfence();
 
   // ---- merge the splits (last block of this (b, kv head)) -------------------
+  // (m_s, l_s) of every used split and head into shared memory (the pipeline buffers
+  // are free now), weights 2^(m_s - M) per head, then O over the splits.
   const int used = min(nsplit, (len + share - 1) / share);       // later splits are empty
-  for (int gg = 0; gg < G; ++gg) {
+  float* sw = reinterpret_cast<float*>(dsm);                     // [G][used] weights
+  float* sl = sw + G * used;                                     // [G][used] sums
+  for (int e = threadIdx.x; e < G * used; e += blockDim.x) {
+    const int gg = e / used, s = e - gg * used;
+    sw[e] = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2);
+    sl[e] = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2 + 1);
+  }
+  __syncthreads();
+  for (int gg = warp; gg < G; gg += kWarps) {
     float M = -INFINITY;
-    for (int s = threadIdx.x; s < used; s += blockDim.x)
-      M = fmaxf(M, __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2));
+    for (int s = lane; s < used; s += 32) M = fmaxf(M, sw[gg * used + s]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    if (lane == 0) s_red[warp] = M;
-    __syncthreads();
-    M = s_red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, s_red[w]);
-    __syncthreads();
     float L = 0.f;
-    for (int s = threadIdx.x; s < used; s += blockDim.x) {
-      const float ms = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2);
-      const float ls = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2 + 1);
+    for (int s = lane; s < used; s += 32) {
+      const float ms = sw[gg * used + s];
       const float wgt = ms == -INFINITY ? 0.f : ex2(ms - M);
-      s_merge_w[s] = wgt;
-      L = fmaf(wgt, ls, L);
+      sw[gg * used + s] = wgt;
+      L = fmaf(wgt, sl[gg * used + s], L);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) s_red[warp] = L;
-    __syncthreads();
-    float tot = 0.f;
+    if (lane == 0) s_inv[gg] = 1.f / L;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int gg = e / D, d = e - gg * D;
+    const float* wrow = sw + gg * used;
+    const float* src = ws_o + (int64_t)pair * nsplit * G * D + (int64_t)gg * D + d;
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    int s = 0;
+    for (; s + 3 < used; s += 4) {
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) tot += s_red[w];
-    const float inv = 1.f / tot;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-      float o0 = 0.f, o1 = 0.f;
-      int s = 0;
-      for (; s + 1 < used; s += 2) {
-        o0 = fmaf(s_merge_w[s], __ldcg(ws_o + (((int64_t)pair * nsplit + s) * G + gg) * D + d), o0);
-        o1 = fmaf(s_merge_w[s + 1], __ldcg(ws_o + (((int64_t)pair * nsplit + s + 1) * G + gg) * D + d), o1);
-      }
-      if (s < used) o0 = fmaf(s_merge_w[s], __ldcg(ws_o + (((int64_t)pair * nsplit + s) * G + gg) * D + d), o0);
-      store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, (o0 + o1) * inv);
+      for (int k = 0; k < 4; ++k) o[k] = fmaf(wrow[s + k], __ldcg(src + (int64_t)(s + k) * G * D), o[k]);
     }
-    __syncthreads();
+    for (; s < used; ++s) o[0] = fmaf(wrow[s], __ldcg(src + (int64_t)s * G * D), o[0]);
+    store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, ((o[0] + o[1]) + (o[2] + o[3])) * s_inv[gg]);
   }
   if (threadIdx.x == 0) tickets[pair] = 0;
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
+cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare) {
+  constexpr size_t smem = dyn_smem_bytes<D, T>();
+  if (prepare) return cudaFuncSetAttribute(k_decode<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
-  k_decode<T, D, G><<<grid, kThreads, 0, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta,
-                                              (float*)c->ws, g, c->scale * 1.4426950408889634f);
+  k_decode<T, D, G><<<grid, kThreads, smem, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta,
+                                                 (float*)c->ws, g, c->scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-cudaError_t launch_d(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
+cudaError_t launch_d(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare) {
   switch (c->cfg.heads / c->cfg.kv_heads) {
-    case 1: return launch_dg<T, D, 1>(c, q, out, s);
-    case 2: return launch_dg<T, D, 2>(c, q, out, s);
-    case 4: return launch_dg<T, D, 4>(c, q, out, s);
-    default: return launch_dg<T, D, 8>(c, q, out, s);
+    case 1: return launch_dg<T, D, 1>(c, q, out, s, prepare);
+    case 2: return launch_dg<T, D, 2>(c, q, out, s, prepare);
+    case 4: return launch_dg<T, D, 4>(c, q, out, s, prepare);
+    default: return launch_dg<T, D, 8>(c, q, out, s, prepare);
   }
 }
 
 template <typename T>
-cudaError_t launch_t(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
-  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, s) : launch_d<T, 128>(c, q, out, s);
+cudaError_t launch_t(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare) {
+  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, s, prepare) : launch_d<T, 128>(c, q, out, s, prepare);
+}
+
+// The decode kernels opt into their dynamic shared memory once per process and
+// device, before their first launch.
+std::mutex g_prep_mu;
+bool g_prepared[64][2][2][4];
+
+cudaError_t prepare_once(kvc_cache* c) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int ti = c->cfg.dtype == KVC_F16 ? 0 : 1, di = c->cfg.head_dim == 64 ? 0 : 1;
+  const int G = c->cfg.heads / c->cfg.kv_heads;
+  const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
+  std::lock_guard<std::mutex> lock(g_prep_mu);
+  if (g_prepared[dev][ti][di][gi]) return cudaSuccess;
+  e = ti == 0 ? launch_t<__half>(c, nullptr, nullptr, 0, true) : launch_t<__nv_bfloat16>(c, nullptr, nullptr, 0, true);
+  if (e == cudaSuccess) g_prepared[dev][ti][di][gi] = true;
+  return e;
 }
 
 }  // namespace
@@ -323,8 +448,13 @@ size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits) {
   return pairs * splits * G * (cfg.head_dim + 2) * 4 + pairs * 4;
 }
 
+cudaError_t kvc_prepare_decode(kvc_cache* c) { return prepare_once(c); }
+
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
-  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, s) : launch_t<__nv_bfloat16>(c, q, out, s);
+  const cudaError_t e = prepare_once(c);
+  if (e != cudaSuccess) return e;
+  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, s, false)
+                                 : launch_t<__nv_bfloat16>(c, q, out, s, false);
 }
 
 // ---------------------------------------------------------------------------

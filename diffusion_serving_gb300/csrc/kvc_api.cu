@@ -109,6 +109,10 @@ int kvc_create(const kvc_config* cfg, void* k_store, void* v_store, void* meta, 
     delete c;
     return KVC_ERR_CUDA;
   }
+  if (c->dec_splits > 0 && kvc_prepare_decode(c) != cudaSuccess) {
+    delete c;
+    return KVC_ERR_CUDA;
+  }
   c->tc_ok = kvc_tc_supported(*cfg) && kvc_tc_make_kv_maps(c);
   cudaStream_t s = as_stream(stream);
   if (cudaMemsetAsync(meta, 0, kvc_meta_bytes(cfg), s) != cudaSuccess ||

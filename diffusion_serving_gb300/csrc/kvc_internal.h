@@ -85,6 +85,7 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
 cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
                                  cudaStream_t s);
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s);
+cudaError_t kvc_prepare_decode(kvc_cache* c);
 bool kvc_decode_supported(const kvc_config& cfg);
 int kvc_internal_check_config(const kvc_config* cfg, int* cap);
 int kvc_internal_decode_splits(const kvc_config& cfg, int cap);
