@@ -409,10 +409,10 @@ def reference(args):
         return
     w = WORKLOADS[args.workload]
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, budget_s=1.0)
+        cpu_oracle_sample(w, budget_s=min(1.0, args.budget_s))
     t_total, flops_total, rows_total = 0.0, 0.0, 0
     for _ in range(args.steps):
-        tf, dt, nrows = cpu_oracle_sample(w, budget_s=5.0)
+        tf, dt, nrows = cpu_oracle_sample(w, budget_s=args.budget_s)
         t_total += dt
         flops_total += tf * 1e12 * dt
         rows_total += nrows
@@ -436,6 +436,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT, choices=sorted(WORKLOADS))
+    ap.add_argument("--budget-s", type=float, default=5.0,
+                    help="seconds of CPU oracle work per step of the reference arm (a bounded sample)")
     ap.add_argument("--pool", type=int, default=8,
                     help="distinct (q, k, v) input sets, reused cyclically over the chunks")
     args = ap.parse_args()
