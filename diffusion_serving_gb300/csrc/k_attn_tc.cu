@@ -554,35 +554,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 }
 
 // ---- host side ----------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// 4-D map over a [d3][d2][d1][128] tensor of 16-bit elements, boxes of 64 x 1 x 128 x 1.
 bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t d1, uint64_t d2, uint64_t d3) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[4] = {(cuuint64_t)kD, d1, d2, d3};
-  const cuuint64_t strides[3] = {kD * 2ull, d1 * kD * 2ull, d2 * d1 * kD * 2ull};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  const CUtensorMapDataType t = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  return enc(m, t, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return kvc_make_tile_map(m, dtype, base, kD, d1, d2, d3, 128);
 }
 
 size_t smem_bytes() { return sizeof(Smem) + 1024; }

@@ -9,15 +9,18 @@
 // Grid (splits, Hkv, B).  Each block takes an equal share (at least kMinShare slots)
 // of the row's kv_len slots; the share is computed on the device from kv_len, so the
 // grid depends only on the shape and a captured graph replays at any length.
-// Inside a block every warp streams its slots once, K and V of several slots in
-// flight per lane, keeping an online softmax (running max m, sum l, accumulator) per
-// q head; the warps' states merge in shared memory into one unnormalised partial
-// (O_s, m_s, l_s) written to the workspace.  The last block of each (b, kv head) to
-// finish (a ticket counter in the workspace, left at zero for the next call) merges
-// the partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+// A producer warp streams the share through a ring of shared-memory stages with TMA
+// tile loads (56 slots x 64 dims per box, 128-byte swizzle): one instruction moves
+// 7 KB, so the whole stream needs a few hundred copy requests per SM.  Seven consumer
+// warps take 8 slots of every 56-slot tile each and keep an online softmax (running
+// max m, sum l, accumulator) per q head; their states merge in shared memory into one
+// unnormalised partial (O_s, m_s, l_s) written to the workspace.  The last block of
+// each (b, kv head) to finish (a ticket counter in the workspace, left at zero for the
+// next call) merges the partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 //
-// Lane mapping: 8 lanes per slot row, each lane holding D/8 consecutive dims
-// (16-byte vector loads), 4 slots per warp instruction.
+// Lane mapping: 8 lanes per slot row, 4 rows per warp instruction; lane sub holds dims
+// {64 v + 8 sub + i : v < D/64, i < 8}, i.e. 16-byte chunk `sub` of each 64-dim box, so
+// the 8 lanes of a row read one whole 128-byte swizzled row (conflict-free).
 #include "kvc_internal.h"
 
 #include <cuda_bf16.h>
@@ -27,11 +30,13 @@
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kMinShare = 64;       // fewest slots a block takes (short prefixes use few splits)
-constexpr int kChunk = 8;           // slots per pipeline stage of a warp (two groups of 4)
-constexpr int kStages = 4;          // stages per warp: 3 chunks in flight while one is consumed
+// 8 warps per block: registers are split over the SM's 4 sub-partitions, so a block of
+// 8 warps may give each thread up to 255 registers (9 warps would cap it at 168).
+constexpr int kWarps = 7;                   // consumer warps, 8 rows of every tile each
+constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
+constexpr int kMinShare = 64;               // fewest slots a block takes (short prefixes use few splits)
+constexpr int kTile = kWarps * 8;           // slots per stage (one TMA box of rows: 7 swizzle atoms)
+constexpr int kStages = 7;                 // 7 x 28 KB in flight per SM (bandwidth x latency)
 constexpr uint64_t kTimeoutNs = 500000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -50,6 +55,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -62,22 +71,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait (0.5 s of %globaltimer); false when it ran out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait (0.5 s of %globaltimer); false when it ran out or the block is aborting.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          bool honour_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 63) == 0 && globaltimer() - t0 > kTimeoutNs) return false;
+    if ((n & 63) == 0) {
+      if (honour_abort && *abort) return false;
+      if (globaltimer() - t0 > kTimeoutNs) {
+        *abort = 1;
+        return false;
+      }
+    }
   }
 }
 
-// One contiguous global -> shared copy on the bulk-copy (TMA) engine, completion
-// counted in bytes on `bar`.  Addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst, int c0, int c1, int c2,
+                                            int c3) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -108,35 +124,34 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-template <int D, typename T>
-__host__ __device__ constexpr size_t stage_bytes() { return (size_t)kChunk * D * sizeof(T) * 2; }   // K and V rows of a chunk
+template <int D>
+__host__ __device__ constexpr uint32_t box_bytes() { return kTile * 128u; }           // kTile slots x 64 dims x 2 B
+template <int D>
+__host__ __device__ constexpr uint32_t stage_bytes() { return 2u * (D / 64) * box_bytes<D>(); }   // K and V
+template <int D>
+__host__ __device__ constexpr size_t dyn_smem_bytes() { return (size_t)kStages * stage_bytes<D>() + 1024; }
 
-template <int D, typename T>
-__host__ __device__ constexpr size_t dyn_smem_bytes() { return (size_t)kWarps * kStages * stage_bytes<D, T>(); }
-
-// Lane mapping: 8 lanes (sub = 0..7) per slot row, 4 rows per warp instruction (grp).
-// Lane sub holds dims {64 v + 8 sub + i : v < D/64, i < 8}, so that the 8 lanes of a
-// group read 128 contiguous bytes of a row per 16-byte load (conflict-free).
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst, const T* __restrict__ vst,
-         int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2) {
-  constexpr int VPL = D / 64;        // 16-byte vectors per lane per row
+k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const T* __restrict__ q,
+         T* __restrict__ out, int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2) {
+  constexpr int VPL = D / 64;        // 16-byte vectors (= 64-dim boxes) per lane per row
   constexpr int EPL = VPL * 8;       // dims per lane
-  constexpr int ROW = D * (int)sizeof(T);
-  constexpr int SB = (int)stage_bytes<D, T>();
-  extern __shared__ __align__(128) uint8_t dsm[];     // [kWarps][kStages][K rows | V rows]
-  __shared__ uint64_t bars[kWarps][kStages];
+  constexpr uint32_t BOX = box_bytes<D>();
+  constexpr uint32_t SB = stage_bytes<D>();
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[kStages], empty[kStages];
   __shared__ float s_acc[kWarps][G][D];
   __shared__ float s_ml[kWarps][G][2];
   __shared__ float s_inv[G];
-  __shared__ int s_last, s_timeout;
+  __shared__ int s_last, s_abort;
 
   const int split = blockIdx.x, nsplit = gridDim.x;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = lane & 7;          // dim slice
-  const int grp = lane >> 3;         // slot within the group of 4
+  const int grp = lane >> 3;         // row within the group of 4
 
   int row0 = 0, len = 0;
   if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;
@@ -146,164 +161,160 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
   share = (share + 15) & ~15;
   const int t0 = split * share;
   const int nt = max(0, min(len, t0 + share) - t0);
+  const int n_tiles = (nt + kTile - 1) / kTile;
 
-  if (threadIdx.x < kWarps * kStages) mbar_init(&bars[0][0] + threadIdx.x, 1);
-  if (threadIdx.x == 0) s_timeout = 0;
+  if (threadIdx.x < kStages) {
+    mbar_init(&full[threadIdx.x], 1);
+    mbar_init(&empty[threadIdx.x], kWarps);
+  }
+  if (threadIdx.x == 0) s_abort = 0;
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
+  volatile int* abort = &s_abort;
 
-  // this warp's chunks: slots [t0 + kChunk (warp + kWarps i), +kChunk) for i = 0, 1, ...
-  const int n_chunks = nt > warp * kChunk ? (nt - warp * kChunk + kWarps * kChunk - 1) / (kWarps * kChunk) : 0;
-  uint8_t* wsm = dsm + (size_t)warp * kStages * SB;
-  const int64_t row_step = (int64_t)g.Hkv * D;         // elements between consecutive slots
-  const T* kbase = kst + kvc_kv_offset(g, b, row0, t0, kvh);
-  const T* vbase = vst + kvc_kv_offset(g, b, row0, t0, kvh);
-  auto issue = [&](int i) {                            // whole warp; lanes 0-15 copy one row each
-    const int st = i % kStages;
-    const int first = (warp + kWarps * i) * kChunk;
-    const int nvalid = min(kChunk, nt - first);
-    if (lane == 0) mbar_expect_tx(&bars[warp][st], (uint32_t)(2 * nvalid * ROW));
-    __syncwarp();
-    const int r = lane & 7;
-    if (lane < 16 && r < nvalid) {
-      const T* src = (lane < 8 ? kbase : vbase) + (int64_t)(first + r) * row_step;
-      bulk_g2s(wsm + st * SB + (lane < 8 ? 0 : kChunk * ROW) + r * ROW, src, ROW, &bars[warp][st]);
+  if (warp == kWarps) {
+    // ---------------- producer: TMA tiles of K and V into the stage ring ----------------
+    if (lane == 0) {
+      const int kv_batch = g.layout == KVC_PACKED ? 0 : b;
+      int issued = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % kStages;
+        if (t >= kStages && !mbar_wait(&empty[st], ((t / kStages) - 1) & 1, abort)) break;
+        mbar_expect_tx(&full[st], SB);
+        uint8_t* dst = dsm + st * SB;
+        const int row = row0 + t0 + t * kTile;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          tma_load_4d(&tm_k, &full[st], dst + v * BOX, v * 64, kvh, row, kv_batch);
+          tma_load_4d(&tm_v, &full[st], dst + (VPL + v) * BOX, v * 64, kvh, row, kv_batch);
+        }
+        issued = t + 1;
+      }
+      if (*abort) {   // let every load issued here land before the block releases its shared memory
+        for (int t = max(0, issued - kStages); t < issued; ++t)
+          mbar_wait(&full[t % kStages], (t / kStages) & 1, abort, false);
+      }
     }
-  };
-  int issued = 0;
-  for (; issued < kStages && issued < n_chunks; ++issued) issue(issued);
+  }
 
   // query slice for this lane's dims, G heads, pre-scaled into the exp2 domain
   float qv[G][EPL];
-#pragma unroll
-  for (int gg = 0; gg < G; ++gg) {
-    const T* qp = q + ((int64_t)b * g.H + kvh * G + gg) * D;
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      uint4 u = __ldg(reinterpret_cast<const uint4*>(qp + 64 * v + 8 * sub));
-      unpack8(u, &qv[gg][8 * v], (const T*)nullptr);
-    }
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) qv[gg][e] *= scale_log2;
-  }
-
   float m[G], l[G], acc[G][EPL];
-#pragma unroll
-  for (int gg = 0; gg < G; ++gg) {
-    m[gg] = -INFINITY;
-    l[gg] = 0.f;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) acc[gg][e] = 0.f;
-  }
-
-  bool ok = true;
-  for (int i = 0; i < n_chunks; ++i) {
-    const int st = i % kStages;
-    ok = __all_sync(0xffffffffu, mbar_wait(&bars[warp][st], (i / kStages) & 1));
-    if (!ok) break;
-    const int first = (warp + kWarps * i) * kChunk;
-    const uint8_t* ks = wsm + st * SB;
-    const uint8_t* vs = ks + kChunk * ROW;
-    float sc[2][G];
-    bool valid[2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int r = u * 4 + grp;
-      valid[u] = first + r < nt;
-      float kf[EPL];
-#pragma unroll
-      for (int v = 0; v < VPL; ++v)
-        unpack8(*reinterpret_cast<const uint4*>(ks + r * ROW + v * 128 + sub * 16), &kf[8 * v], (const T*)nullptr);
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        float2 a2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int e = 0; e < EPL; e += 2)
-          a2 = __ffma2_rn(make_float2(qv[gg][e], qv[gg][e + 1]), make_float2(kf[e], kf[e + 1]), a2);
-        float a = a2.x + a2.y;
-        a += __shfl_xor_sync(0xffffffffu, a, 1);
-        a += __shfl_xor_sync(0xffffffffu, a, 2);
-        a += __shfl_xor_sync(0xffffffffu, a, 4);
-        sc[u][gg] = valid[u] ? a : -INFINITY;
-      }
-    }
-    float vf[2][EPL];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int r = u * 4 + grp;
-#pragma unroll
-      for (int v = 0; v < VPL; ++v)
-        unpack8(*reinterpret_cast<const uint4*>(vs + r * ROW + v * 128 + sub * 16), &vf[u][8 * v], (const T*)nullptr);
-    }
-    if (first + kChunk > nt) {                           // the warp's last, partial chunk
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) vf[u][e] = valid[u] ? vf[u][e] : 0.f;   // stale rows past nt
-    }
-    __syncwarp();
-    if (issued < n_chunks) issue(issued++);             // refill this stage (chunk i + kStages) while computing
+  if (warp < kWarps) {
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
-      float mx = fmaxf(sc[0][gg], sc[1][gg]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      if (mx > m[gg]) {                                  // warp-uniform: the running max grows
-        const float alpha = ex2(m[gg] - mx);             // 0 on the first chunk (m = -inf)
-        m[gg] = mx;
-        l[gg] *= alpha;
+      const T* qp = q + ((int64_t)b * g.H + kvh * G + gg) * D;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        uint4 u = __ldg(reinterpret_cast<const uint4*>(qp + 64 * v + 8 * sub));
+        unpack8(u, &qv[gg][8 * v], (const T*)nullptr);
+      }
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) qv[gg][e] *= scale_log2;
+      m[gg] = -INFINITY;
+      l[gg] = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) acc[gg][e] = 0.f;
+    }
+
+    for (int t = 0; t < n_tiles; ++t) {
+      const int st = t % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (t / kStages) & 1, abort))) break;
+      const uint8_t* kst = dsm + st * SB;
+      const uint8_t* vst = kst + VPL * BOX;
+      const int first = t * kTile + warp * 8;          // this warp's 8 rows of the tile
+      float sc[2][G];
+      bool valid[2];
+      float vf[2][EPL];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int r = warp * 8 + u * 4 + grp;           // row within the tile
+        valid[u] = first + u * 4 + grp < nt;
+        const uint32_t off = r * 128 + ((sub ^ (r & 7)) << 4);   // 128B swizzle: 16-byte chunk sub of row r
+        float kf[EPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          unpack8(*reinterpret_cast<const uint4*>(kst + v * BOX + off), &kf[8 * v], (const T*)nullptr);
+          unpack8(*reinterpret_cast<const uint4*>(vst + v * BOX + off), &vf[u][8 * v], (const T*)nullptr);
+        }
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int e = 0; e < EPL; e += 2)
+            a2 = __ffma2_rn(make_float2(qv[gg][e], qv[gg][e + 1]), make_float2(kf[e], kf[e + 1]), a2);
+          float a = a2.x + a2.y;
+          a += __shfl_xor_sync(0xffffffffu, a, 1);
+          a += __shfl_xor_sync(0xffffffffu, a, 2);
+          a += __shfl_xor_sync(0xffffffffu, a, 4);
+          sc[u][gg] = valid[u] ? a : -INFINITY;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);           // this warp is done with the stage
+      if (first >= nt) continue;                         // nothing of this warp in the tile's tail
+      if (first + 8 > nt) {                              // partial rows: stale data past nt
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) vf[u][e] = valid[u] ? vf[u][e] : 0.f;
+      }
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        float mx = fmaxf(sc[0][gg], sc[1][gg]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (mx > m[gg]) {                                // warp-uniform: the running max grows
+          const float alpha = ex2(m[gg] - mx);           // 0 on the first tile (m = -inf)
+          m[gg] = mx;
+          l[gg] *= alpha;
+#pragma unroll
+          for (int e = 0; e < EPL; e += 2) {
+            const float2 y = __fmul2_rn(make_float2(acc[gg][e], acc[gg][e + 1]), make_float2(alpha, alpha));
+            acc[gg][e] = y.x;
+            acc[gg][e + 1] = y.y;
+          }
+        }
+        const float p0 = ex2(sc[0][gg] - m[gg]), p1 = ex2(sc[1][gg] - m[gg]);
+        l[gg] += p0 + p1;
 #pragma unroll
         for (int e = 0; e < EPL; e += 2) {
-          const float2 y = __fmul2_rn(make_float2(acc[gg][e], acc[gg][e + 1]), make_float2(alpha, alpha));
+          float2 y = make_float2(acc[gg][e], acc[gg][e + 1]);
+          y = __ffma2_rn(make_float2(p0, p0), make_float2(vf[0][e], vf[0][e + 1]), y);
+          y = __ffma2_rn(make_float2(p1, p1), make_float2(vf[1][e], vf[1][e + 1]), y);
           acc[gg][e] = y.x;
           acc[gg][e + 1] = y.y;
         }
       }
-      const float p0 = ex2(sc[0][gg] - m[gg]), p1 = ex2(sc[1][gg] - m[gg]);
-      l[gg] += p0 + p1;
-#pragma unroll
-      for (int e = 0; e < EPL; e += 2) {
-        float2 y = make_float2(acc[gg][e], acc[gg][e + 1]);
-        y = __ffma2_rn(make_float2(p0, p0), make_float2(vf[0][e], vf[0][e + 1]), y);
-        y = __ffma2_rn(make_float2(p1, p1), make_float2(vf[1][e], vf[1][e + 1]), y);
-        acc[gg][e] = y.x;
-        acc[gg][e + 1] = y.y;
-      }
     }
-  }
-  if (!ok) {
-    // give up: record it, then let this warp's copies in flight land before the block exits
-    if (lane == 0) s_timeout = 1;
-    for (int c = max(0, issued - kStages); c < issued; ++c)   // newest chunk issued to each stage
-      mbar_wait(&bars[warp][c % kStages], (c / kStages) & 1);
-  }
-  // Sum the warp's 4 slot groups (they share m).  Every lane of a group added the
-  // same p values to l, so after the sum any lane holds the warp's total.
-#pragma unroll
-  for (int gg = 0; gg < G; ++gg) {
-    l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 8);
-    l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 16);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) {
-      float a = acc[gg][e];
-      a += __shfl_xor_sync(0xffffffffu, a, 8);
-      a += __shfl_xor_sync(0xffffffffu, a, 16);
-      acc[gg][e] = a;
-    }
-  }
-  if (grp == 0) {
+    // Sum the warp's 4 row groups (they share m).  Every lane of a group added the same
+    // p values to l, so after the sum any lane holds the warp's total.
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
+      l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 8);
+      l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 16);
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) s_acc[warp][gg][(e >> 3) * 64 + sub * 8 + (e & 7)] = acc[gg][e];
-      if (sub == 0) {
-        s_ml[warp][gg][0] = m[gg];
-        s_ml[warp][gg][1] = l[gg];
+      for (int e = 0; e < EPL; ++e) {
+        float a = acc[gg][e];
+        a += __shfl_xor_sync(0xffffffffu, a, 8);
+        a += __shfl_xor_sync(0xffffffffu, a, 16);
+        acc[gg][e] = a;
+      }
+    }
+    if (grp == 0) {
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) s_acc[warp][gg][(e >> 3) * 64 + sub * 8 + (e & 7)] = acc[gg][e];
+        if (sub == 0) {
+          s_ml[warp][gg][0] = m[gg];
+          s_ml[warp][gg][1] = l[gg];
+        }
       }
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && s_timeout) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
+  if (threadIdx.x == 0 && s_abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 
   // ---- this block's partial: merge the warps ---------------------------------
   const int pairs = g.B * g.Hkv;
@@ -343,8 +354,8 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
   __threadfence();
 
   // ---- merge the splits (last block of this (b, kv head)) -------------------
-  // (m_s, l_s) of every used split and head into shared memory (the pipeline buffers
-  // are free now), weights 2^(m_s - M) per head, then O over the splits.
+  // (m_s, l_s) of every used split and head into shared memory (the stage ring is free
+  // now), weights 2^(m_s - M) per head, then O over the splits.
   const int used = min(nsplit, (len + share - 1) / share);       // later splits are empty
   float* sw = reinterpret_cast<float*>(dsm);                     // [G][used] weights
   float* sl = sw + G * used;                                     // [G][used] sums
@@ -354,7 +365,7 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
     sl[e] = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2 + 1);
   }
   __syncthreads();
-  for (int gg = warp; gg < G; gg += kWarps) {
+  for (int gg = warp; gg < G; gg += kWarps + 1) {
     float M = -INFINITY;
     for (int s = lane; s < used; s += 32) M = fmaxf(M, sw[gg * used + s]);
 #pragma unroll
@@ -389,13 +400,13 @@ k_decode(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst
 
 template <typename T, int D, int G>
 cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare) {
-  constexpr size_t smem = dyn_smem_bytes<D, T>();
+  constexpr size_t smem = dyn_smem_bytes<D>();
   if (prepare) return cudaFuncSetAttribute(k_decode<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
-  k_decode<T, D, G><<<grid, kThreads, smem, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta,
-                                                 (float*)c->ws, g, c->scale * 1.4426950408889634f);
+  k_decode<T, D, G><<<grid, kThreads, smem, s>>>(c->tm_dk, c->tm_dv, (const T*)q, (T*)out, c->meta, (float*)c->ws, g,
+                                                 c->scale * 1.4426950408889634f);
   return cudaGetLastError();
 }
 
@@ -449,6 +460,13 @@ size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits) {
 }
 
 cudaError_t kvc_prepare_decode(kvc_cache* c) { return prepare_once(c); }
+
+bool kvc_make_decode_maps(kvc_cache* c) {
+  const kvc_config& g = c->cfg;
+  const uint64_t batches = g.layout == KVC_PACKED ? 1 : (uint64_t)g.batch;
+  return kvc_make_tile_map(&c->tm_dk, g.dtype, c->k, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile) &&
+         kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile);
+}
 
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
   const cudaError_t e = prepare_once(c);
@@ -529,6 +547,7 @@ extern "C" int kvc_attend_decode_noalloc(const kvc_config* cfg, const void* k_st
   c.meta = meta;
   c.ws = scratch;
   c.dec_splits = splits;
+  if (!kvc_make_decode_maps(&c)) return KVC_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the tickets sit after the partials; an earlier call with another shape may have
   // left partial data there

@@ -11,9 +11,9 @@
 
 namespace {
 
-// Blocks the split-KV decode kernel aims for (about two per SM of a 152-SM GB300).
+// Blocks the split-KV decode kernel aims for (one per SM of a 152-SM GB300).
 // A constant, so that workspace sizes do not depend on the device queried.
-constexpr int kDecodeTargetBlocks = 304;
+constexpr int kDecodeTargetBlocks = 152;
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
@@ -60,6 +60,40 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 int launched(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
 
 }  // namespace
+
+// ---- TMA descriptors ---------------------------------------------------------
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+}  // namespace
+
+bool kvc_make_tile_map(CUtensorMap* m, int dtype, const void* base, int D, uint64_t d1, uint64_t d2, uint64_t d3,
+                       uint32_t box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr || (dtype != KVC_BF16 && dtype != KVC_F16)) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, d1, d2, d3};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2ull, d1 * D * 2ull, d2 * d1 * D * 2ull};
+  const cuuint32_t box[4] = {64, 1, box_rows, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return enc(m, t, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int kvc_internal_check_config(const kvc_config* cfg, int* cap) { return check_cfg(cfg, cap); }
 int kvc_internal_decode_splits(const kvc_config& cfg, int cap) { return decode_splits(cfg, cap); }
@@ -109,7 +143,7 @@ int kvc_create(const kvc_config* cfg, void* k_store, void* v_store, void* meta, 
     delete c;
     return KVC_ERR_CUDA;
   }
-  if (c->dec_splits > 0 && kvc_prepare_decode(c) != cudaSuccess) {
+  if (c->dec_splits > 0 && (!kvc_make_decode_maps(c) || kvc_prepare_decode(c) != cudaSuccess)) {
     delete c;
     return KVC_ERR_CUDA;
   }

@@ -30,8 +30,10 @@ struct kvc_cache {
   int num_sms;
   int dec_splits;     // split-KV decode: splits per (row, kv head); 0 = no decode kernel
   bool tc_ok;         // the tensor-core chunk kernel serves this config
-  CUtensorMap tm_k;   // K store, 128B-swizzled 64x128 boxes (tensor-core kernel)
+  CUtensorMap tm_k;   // K store, 128B-swizzled boxes of 64 dims x 128 slots (tensor-core kernel)
   CUtensorMap tm_v;   // V store, same boxes
+  CUtensorMap tm_dk;  // K store, boxes of 64 dims x 64 slots (decode kernel)
+  CUtensorMap tm_dv;  // V store, same boxes
 };
 
 // Row geometry of the store as seen by the attention kernels: row b's slot j lives
@@ -94,3 +96,10 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
                                cudaStream_t s);
 bool kvc_tc_supported(const kvc_config& cfg);
 bool kvc_tc_make_kv_maps(kvc_cache* c);
+// 4-D TMA map over a 16-bit tensor [d3][d2][d1][D] (D = 64 or 128), 128B-swizzled boxes
+// of 64 x 1 x box_rows x 1 elements.  False if the driver entry point is missing or the
+// encoding is rejected.
+bool kvc_make_tile_map(CUtensorMap* m, int dtype, const void* base, int D, uint64_t d1, uint64_t d2, uint64_t d3,
+                       uint32_t box_rows);
+// Decode maps of a store (tm_dk, tm_dv) for the config in c.
+bool kvc_make_decode_maps(kvc_cache* c);
