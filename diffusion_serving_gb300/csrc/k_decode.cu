@@ -10,9 +10,10 @@
 // of the row's kv_len slots; the share is computed on the device from kv_len, so the
 // grid depends only on the shape and a captured graph replays at any length.
 // A producer warp streams the share through a ring of shared-memory stages with TMA
-// tile loads (56 slots x 64 dims per box, 128-byte swizzle): one instruction moves
-// 7 KB, so the whole stream needs a few hundred copy requests per SM.  Seven consumer
-// warps take 8 slots of every 56-slot tile each and keep an online softmax (running
+// tile loads (112 slots x 64 dims per box, 128-byte swizzle): one instruction moves
+// 14 KB, so the whole stream needs a few hundred copy requests per SM.  Seven consumer
+// warps take 16 slots of every 112-slot tile each, as 4 independent row groups whose
+// loads and dot products overlap and keep an online softmax (running
 // max m, sum l, accumulator) per q head; their states merge in shared memory into one
 // unnormalised partial (O_s, m_s, l_s) written to the workspace.  The last block of
 // each (b, kv head) to finish (a ticket counter in the workspace, left at zero for the
@@ -32,11 +33,13 @@ namespace {
 
 // 8 warps per block: registers are split over the SM's 4 sub-partitions, so a block of
 // 8 warps may give each thread up to 255 registers (9 warps would cap it at 168).
-constexpr int kWarps = 7;                   // consumer warps, 8 rows of every tile each
+constexpr int kWarps = 7;                   // consumer warps
+constexpr int kGroups = 4;                  // row groups of 4 per consumer warp per tile
+constexpr int kRowsPerWarp = kGroups * 4;   // 16 rows of every tile per consumer warp
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
 constexpr int kMinShare = 64;               // fewest slots a block takes (short prefixes use few splits)
-constexpr int kTile = kWarps * 8;           // slots per stage (one TMA box of rows: 7 swizzle atoms)
-constexpr int kStages = 7;                 // 7 x 28 KB in flight per SM (bandwidth x latency)
+constexpr int kTile = kWarps * kRowsPerWarp;  // 112 slots per stage (one TMA box of rows: 14 swizzle atoms)
+constexpr int kStages = 3;                  // 3 x 56 KB in flight per SM (bandwidth x latency)
 constexpr uint64_t kTimeoutNs = 500000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -222,70 +225,89 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (t / kStages) & 1, abort))) break;
       const uint8_t* kst = dsm + st * SB;
       const uint8_t* vst = kst + VPL * BOX;
-      const int first = t * kTile + warp * 8;          // this warp's 8 rows of the tile
-      float sc[2][G];
-      bool valid[2];
-      float vf[2][EPL];
+      const int first = t * kTile + warp * kRowsPerWarp;   // this warp's rows of the tile
+      if (first < nt) {
+        // scores of the warp's kGroups row groups (independent: they overlap in flight)
+        float sc[kGroups][G];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int r = warp * 8 + u * 4 + grp;           // row within the tile
-        valid[u] = first + u * 4 + grp < nt;
-        const uint32_t off = r * 128 + ((sub ^ (r & 7)) << 4);   // 128B swizzle: 16-byte chunk sub of row r
-        float kf[EPL];
+        for (int u = 0; u < kGroups; ++u) {
+          const int r = warp * kRowsPerWarp + u * 4 + grp;          // row within the tile
+          const uint32_t off = r * 128 + ((sub ^ (r & 7)) << 4);     // 128B swizzle: chunk `sub` of row r
+          float kf[EPL];
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-          unpack8(*reinterpret_cast<const uint4*>(kst + v * BOX + off), &kf[8 * v], (const T*)nullptr);
-          unpack8(*reinterpret_cast<const uint4*>(vst + v * BOX + off), &vf[u][8 * v], (const T*)nullptr);
+          for (int v = 0; v < VPL; ++v)
+            unpack8(*reinterpret_cast<const uint4*>(kst + v * BOX + off), &kf[8 * v], (const T*)nullptr);
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg) {
+            float2 a2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2)
+              a2 = __ffma2_rn(make_float2(qv[gg][e], qv[gg][e + 1]), make_float2(kf[e], kf[e + 1]), a2);
+            sc[u][gg] = a2.x + a2.y;
+          }
         }
 #pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          float2 a2 = make_float2(0.f, 0.f);
+        for (int u = 0; u < kGroups; ++u)
 #pragma unroll
-          for (int e = 0; e < EPL; e += 2)
-            a2 = __ffma2_rn(make_float2(qv[gg][e], qv[gg][e + 1]), make_float2(kf[e], kf[e + 1]), a2);
-          float a = a2.x + a2.y;
-          a += __shfl_xor_sync(0xffffffffu, a, 1);
-          a += __shfl_xor_sync(0xffffffffu, a, 2);
-          a += __shfl_xor_sync(0xffffffffu, a, 4);
-          sc[u][gg] = valid[u] ? a : -INFINITY;
+          for (int gg = 0; gg < G; ++gg) {
+            float a = sc[u][gg];
+            a += __shfl_xor_sync(0xffffffffu, a, 1);
+            a += __shfl_xor_sync(0xffffffffu, a, 2);
+            a += __shfl_xor_sync(0xffffffffu, a, 4);
+            sc[u][gg] = first + u * 4 + grp < nt ? a : -INFINITY;
+          }
+        // online softmax update per head, then P.V with V re-read from shared memory
+        float p[kGroups][G];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          float mx = sc[0][gg];
+#pragma unroll
+          for (int u = 1; u < kGroups; ++u) mx = fmaxf(mx, sc[u][gg]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          if (mx > m[gg]) {                                // warp-uniform: the running max grows
+            const float alpha = ex2(m[gg] - mx);           // 0 on the first tile (m = -inf)
+            m[gg] = mx;
+            l[gg] *= alpha;
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+              const float2 y = __fmul2_rn(make_float2(acc[gg][e], acc[gg][e + 1]), make_float2(alpha, alpha));
+              acc[gg][e] = y.x;
+              acc[gg][e + 1] = y.y;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < kGroups; ++u) {
+            p[u][gg] = ex2(sc[u][gg] - m[gg]);
+            l[gg] += p[u][gg];
+          }
+        }
+        const bool partial = first + kRowsPerWarp > nt;     // stale rows past nt: their V is zeroed
+#pragma unroll
+        for (int u = 0; u < kGroups; ++u) {
+          const int r = warp * kRowsPerWarp + u * 4 + grp;
+          const uint32_t off = r * 128 + ((sub ^ (r & 7)) << 4);
+          float vf[EPL];
+#pragma unroll
+          for (int v = 0; v < VPL; ++v)
+            unpack8(*reinterpret_cast<const uint4*>(vst + v * BOX + off), &vf[8 * v], (const T*)nullptr);
+          if (partial && first + u * 4 + grp >= nt) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) vf[e] = 0.f;
+          }
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg)
+#pragma unroll
+            for (int e = 0; e < EPL; e += 2) {
+              const float2 y = __ffma2_rn(make_float2(p[u][gg], p[u][gg]), make_float2(vf[e], vf[e + 1]),
+                                          make_float2(acc[gg][e], acc[gg][e + 1]));
+              acc[gg][e] = y.x;
+              acc[gg][e + 1] = y.y;
+            }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);           // this warp is done with the stage
-      if (first >= nt) continue;                         // nothing of this warp in the tile's tail
-      if (first + 8 > nt) {                              // partial rows: stale data past nt
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-          for (int e = 0; e < EPL; ++e) vf[u][e] = valid[u] ? vf[u][e] : 0.f;
-      }
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        float mx = fmaxf(sc[0][gg], sc[1][gg]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        if (mx > m[gg]) {                                // warp-uniform: the running max grows
-          const float alpha = ex2(m[gg] - mx);           // 0 on the first tile (m = -inf)
-          m[gg] = mx;
-          l[gg] *= alpha;
-#pragma unroll
-          for (int e = 0; e < EPL; e += 2) {
-            const float2 y = __fmul2_rn(make_float2(acc[gg][e], acc[gg][e + 1]), make_float2(alpha, alpha));
-            acc[gg][e] = y.x;
-            acc[gg][e + 1] = y.y;
-          }
-        }
-        const float p0 = ex2(sc[0][gg] - m[gg]), p1 = ex2(sc[1][gg] - m[gg]);
-        l[gg] += p0 + p1;
-#pragma unroll
-        for (int e = 0; e < EPL; e += 2) {
-          float2 y = make_float2(acc[gg][e], acc[gg][e + 1]);
-          y = __ffma2_rn(make_float2(p0, p0), make_float2(vf[0][e], vf[0][e + 1]), y);
-          y = __ffma2_rn(make_float2(p1, p1), make_float2(vf[1][e], vf[1][e + 1]), y);
-          acc[gg][e] = y.x;
-          acc[gg][e + 1] = y.y;
-        }
-      }
     }
     // Sum the warp's 4 row groups (they share m).  Every lane of a group added the same
     // p values to l, so after the sum any lane holds the warp's total.
