@@ -13,6 +13,9 @@
 //                captured graph write the slot the device holds.
 #include "kvc_internal.h"
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 namespace {
 
 __global__ void k_advance(int32_t* __restrict__ meta, int B, int row, int n, int layout, int sink,
@@ -143,6 +146,114 @@ k_write(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* _
   }
 }
 
+// Write with RoPE fused into the K half: K rows are rotated at their absolute position
+// before they are stored, V rows are copied unchanged (flashdreams issue "add an opt-in
+// circular KV policy for streaming attention", "proposed boundary": absolute positions
+// determine RoPE before storage).  Pair j of a head, (x[2j], x[2j+1]), turns by the
+// angle whose (cos, sin) the caller's table holds at [pos][j]:
+//   (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos), fp32 FMAs, rounded to the store type.
+// Absolute position of token i: CIRCULAR (chunks - 1) * chunk + i; LINEAR base + i, or
+// slots[i] when slots are given; PACKED i.  Rows whose position is outside the table
+// are skipped and set KVC_DEV_BAD_POS.
+template <typename T> struct Pack;
+template <> struct Pack<__nv_bfloat16> {
+  static constexpr int kPairs = 4;   // pairs per 16-byte vector
+  __device__ static void rot(uint4& u, const float2* cs) {
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __bfloat1622float2(h[i]);
+      const float2 c = cs[i];
+      h[i] = __floats2bfloat162_rn(fmaf(x.x, c.x, -x.y * c.y), fmaf(x.x, c.y, x.y * c.x));
+    }
+  }
+};
+template <> struct Pack<__half> {
+  static constexpr int kPairs = 4;
+  __device__ static void rot(uint4& u, const float2* cs) {
+    __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 x = __half22float2(h[i]);
+      const float2 c = cs[i];
+      h[i] = __floats2half2_rn(fmaf(x.x, c.x, -x.y * c.y), fmaf(x.x, c.y, x.y * c.x));
+    }
+  }
+};
+template <> struct Pack<float> {
+  static constexpr int kPairs = 2;
+  __device__ static void rot(uint4& u, const float2* cs) {
+    float* f = reinterpret_cast<float*>(&u);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float x0 = f[2 * i], x1 = f[2 * i + 1];
+      const float2 c = cs[i];
+      f[2 * i] = fmaf(x0, c.x, -x1 * c.y);
+      f[2 * i + 1] = fmaf(x0, c.y, x1 * c.x);
+    }
+  }
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kWriteThreads)
+k_write_rope(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* __restrict__ kdst,
+             uint4* __restrict__ vdst, int32_t* __restrict__ meta, const int32_t* __restrict__ slots,
+             const float2* __restrict__ rope, int rope_positions, int B, int n, int row_vecs, int cap, int layout,
+             int chunk, int head_dim) {
+  constexpr int P = Pack<T>::kPairs;
+  const int lane = threadIdx.x & 31;
+  const int rows_per_tensor = B * n;
+  const int rows = 2 * rows_per_tensor;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  const int half_d = head_dim / 2;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+    const int t = r >= rows_per_tensor;
+    const int e = r - (t ? rows_per_tensor : 0);
+    const int b = e / n;
+    const int i = e - b * n;
+    int64_t drow = -1;
+    int pos = -1;
+    if (layout == KVC_PACKED) {
+      const int32_t* cu = meta + kvc_meta_cu(B);
+      const int lo = cu[b], hi = cu[b + 1];
+      if (i < hi - lo && lo >= 0 && hi <= cap) drow = lo + i;
+      pos = i;
+    } else if (slots != nullptr) {
+      const int sl = slots[i];
+      if (sl >= 0 && sl < cap) drow = (int64_t)b * cap + sl;
+      else if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_SLOT);
+      pos = sl;
+    } else {
+      const int32_t* m = meta + kvc_meta_row(b);
+      const int chunks = m[KVC_ROW_CHUNKS];
+      const int sl = m[KVC_ROW_BASE] + i;
+      const bool ok = chunks > 0 && sl >= 0 && sl < cap && (layout != KVC_LINEAR || sl < m[KVC_ROW_FILLED]);
+      if (ok) drow = (int64_t)b * cap + sl;
+      else if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, chunks > 0 ? KVC_DEV_BAD_SLOT : KVC_DEV_NO_CHUNK);
+      pos = layout == KVC_CIRCULAR ? (chunks - 1) * chunk + i : sl;
+    }
+    if (drow < 0) continue;
+    if (pos < 0 || pos >= rope_positions) {        // neither K nor V of such a token is written
+      if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_POS);
+      continue;
+    }
+    const uint4* src = (t ? vsrc : ksrc) + (int64_t)e * row_vecs;
+    uint4* dst = (t ? vdst : kdst) + drow * row_vecs;
+    const float2* cs_row = rope + (int64_t)pos * half_d;
+    for (int v = lane; v < row_vecs; v += 32) {
+      uint4 val = __ldg(src + v);
+      if (t == 0) {
+        const int pair0 = (v * P) % half_d;        // first pair of this vector within its head
+        float2 cs[P];
+#pragma unroll
+        for (int k = 0; k < P; ++k) cs[k] = __ldg(cs_row + pair0 + k);
+        Pack<T>::rot(val, cs);
+      }
+      dst[v] = val;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t kvc_launch_advance(kvc_cache* c, int row, int n, cudaStream_t s) {
@@ -172,5 +283,25 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
   if (blocks < 1) blocks = 1;
   k_write<<<(unsigned)blocks, kWriteThreads, 0, s>>>((const uint4*)k, (const uint4*)v, (uint4*)c->k, (uint4*)c->v,
                                                      c->meta, slots, g.batch, n, row_vecs, c->cap, g.layout);
+  return cudaGetLastError();
+}
+
+cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
+                                  const float* rope, int rope_positions, cudaStream_t s) {
+  const kvc_config& g = c->cfg;
+  const int row_vecs = g.kv_heads * g.head_dim * c->eb / 16;
+  const int64_t rows = 2LL * g.batch * n;
+  int64_t blocks = (rows + kWriteThreads / 32 - 1) / (kWriteThreads / 32);
+  const int64_t max_blocks = (int64_t)c->num_sms * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (blocks < 1) blocks = 1;
+#define KVC_WR(T)                                                                                               \
+  k_write_rope<T><<<(unsigned)blocks, kWriteThreads, 0, s>>>(                                                   \
+      (const uint4*)k, (const uint4*)v, (uint4*)c->k, (uint4*)c->v, c->meta, slots, (const float2*)rope,         \
+      rope_positions, g.batch, n, row_vecs, c->cap, g.layout, g.chunk, g.head_dim)
+  if (g.dtype == KVC_F32) KVC_WR(float);
+  else if (g.dtype == KVC_F16) KVC_WR(__half);
+  else KVC_WR(__nv_bfloat16);
+#undef KVC_WR
   return cudaGetLastError();
 }

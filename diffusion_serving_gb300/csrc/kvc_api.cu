@@ -187,6 +187,20 @@ int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, cons
   return launched(kvc_launch_write(c, k, v, n_tokens, d_slots, as_stream(stream)));
 }
 
+int kvc_write_rope(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, const int32_t* d_slots,
+                   const float* d_rope, int32_t rope_positions, void* stream) {
+  if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;
+  if (d_rope == nullptr || ((uintptr_t)d_rope & 7u) != 0 || rope_positions < 1) return KVC_ERR_ARG;
+  if (n_tokens > c->cap && c->cfg.layout != KVC_PACKED) return KVC_ERR_RANGE;
+  if (d_slots != nullptr) {
+    if (c->cfg.layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;
+    if (((uintptr_t)d_slots & 3u) != 0) return KVC_ERR_ARG;
+  } else if (c->cfg.layout == KVC_CIRCULAR && n_tokens != c->cfg.chunk) {
+    return KVC_ERR_ARG;
+  }
+  return launched(kvc_launch_write_rope(c, k, v, n_tokens, d_slots, d_rope, rope_positions, as_stream(stream)));
+}
+
 int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_seqlens, void* stream) {
   if (c == nullptr || (d_kv_len == nullptr && d_cu_seqlens == nullptr)) return KVC_ERR_ARG;
   if (d_kv_len != nullptr && c->cfg.layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;

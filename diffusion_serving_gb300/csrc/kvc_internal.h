@@ -84,6 +84,8 @@ cudaError_t kvc_launch_reset(kvc_cache* c, int row, cudaStream_t s);
 cudaError_t kvc_launch_set_lengths(kvc_cache* c, const int32_t* kv_len, const int32_t* cu, cudaStream_t s);
 cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
                              cudaStream_t s);
+cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
+                                  const float* rope, int rope_positions, cudaStream_t s);
 cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
                                  cudaStream_t s);
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s);

@@ -24,7 +24,7 @@ F32, F16, BF16 = 0, 1, 2
 LINEAR, CIRCULAR, PACKED = 0, 1, 2
 CAUSAL, KERNEL_SIMT = 1, 256
 OK, ERR_ARG, ERR_UNSUPPORTED, ERR_RANGE, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5
-DEV_BAD_SLOT, DEV_BAD_KVLEN, DEV_BAD_CUSEQ, DEV_OVERFLOW, DEV_NO_CHUNK, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
+DEV_BAD_SLOT, DEV_BAD_KVLEN, DEV_BAD_CUSEQ, DEV_OVERFLOW, DEV_NO_CHUNK, DEV_TIMEOUT, DEV_BAD_POS = 1, 2, 4, 8, 16, 32, 64
 META_ROW0 = 4
 
 DTYPE_CODE = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
@@ -57,6 +57,7 @@ def _load():
         "kvc_create": (ctypes.c_int, [cfgp, P, P, P, P, P, ctypes.POINTER(P)]),
         "kvc_advance": (ctypes.c_int, [P, I32, I32, P]),
         "kvc_write": (ctypes.c_int, [P, P, P, I32, P, P]),
+        "kvc_write_rope": (ctypes.c_int, [P, P, P, I32, P, P, I32, P]),
         "kvc_set_lengths": (ctypes.c_int, [P, P, P, P]),
         "kvc_attend": (ctypes.c_int, [P, P, P, I32, U32, P]),
         "kvc_reset": (ctypes.c_int, [P, I32, P]),
@@ -138,6 +139,11 @@ def kvc_write(h: int, k, v, n_tokens: int, slots=None, stream=None) -> None:
     _check(_lib.kvc_write(h, _ptr(k), _ptr(v), n_tokens, _ptr(slots), _stream(stream)), "kvc_write")
 
 
+def kvc_write_rope(h: int, k, v, n_tokens: int, rope, rope_positions: int, slots=None, stream=None) -> None:
+    _check(_lib.kvc_write_rope(h, _ptr(k), _ptr(v), n_tokens, _ptr(slots), _ptr(rope), rope_positions,
+                               _stream(stream)), "kvc_write_rope")
+
+
 def kvc_set_lengths(h: int, kv_len=None, cu_seqlens=None, stream=None) -> None:
     _check(_lib.kvc_set_lengths(h, _ptr(kv_len), _ptr(cu_seqlens), _stream(stream)), "kvc_set_lengths")
 
@@ -202,6 +208,10 @@ class KVCache:
 
     def write(self, k, v, slots=None, stream=None):
         kvc_write(self.handle, k, v, k.shape[1], slots, stream)
+
+    def write_rope(self, k, v, rope, slots=None, stream=None):
+        """Write with K rotated by the (cos, sin) table ``rope`` [positions, D/2, 2] fp32."""
+        kvc_write_rope(self.handle, k, v, k.shape[1], rope, rope.shape[0], slots, stream)
 
     def set_lengths(self, kv_len=None, cu_seqlens=None, stream=None):
         kvc_set_lengths(self.handle, kv_len, cu_seqlens, stream)

@@ -97,6 +97,15 @@ def rope_rotate(x: torch.Tensor, positions, theta: float = 1e4) -> torch.Tensor:
     return out.to(x.dtype)
 
 
+def rope_table(n_positions: int, head_dim: int, theta: float = 1e4) -> torch.Tensor:
+    """(cos, sin) of pos * theta^(-2j/D) for every position and pair j, fp64 rounded to
+    fp32: shape [n_positions, D/2, 2].  The table a model precomputes once."""
+    pos = torch.arange(n_positions, dtype=torch.float64)[:, None]
+    inv = theta ** (-torch.arange(0, head_dim, 2, dtype=torch.float64) / head_dim)[None, :]
+    ang = pos * inv
+    return torch.stack([torch.cos(ang), torch.sin(ang)], dim=-1).to(torch.float32).contiguous()
+
+
 def chunk_inputs(w: Workload, chunk: int, rewrite: int, n_q: int | None = None,
                  n_kv: int | None = None, device="cpu", rope_positions=None):
     """(q, k, v) for one write+attend of workload ``w``.

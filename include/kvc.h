@@ -88,7 +88,8 @@ enum {
   KVC_DEV_BAD_CUSEQ = 4,    /* cu_seqlens not increasing from 0 or beyond capacity  */
   KVC_DEV_OVERFLOW = 8,     /* LINEAR advance past capacity                         */
   KVC_DEV_NO_CHUNK = 16,    /* write with no reserved chunk                         */
-  KVC_DEV_TIMEOUT = 32      /* a bounded in-kernel wait gave up (the kernel returned) */
+  KVC_DEV_TIMEOUT = 32,     /* a bounded in-kernel wait gave up (the kernel returned) */
+  KVC_DEV_BAD_POS = 64      /* kvc_write_rope: a token position outside the rope table  */
 };
 
 /* Attention flags. */
@@ -148,6 +149,20 @@ int kvc_advance(kvc_cache* c, int32_t row, int32_t n_tokens, void* stream);
  * KVC_ERR_ARG for a circular write whose n_tokens differs from `chunk`. */
 int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
               const int32_t* d_slots, void* stream);
+
+/* kvc_write with RoPE fused into the K half: each K row is rotated at its absolute
+ * position before it is stored; V rows are copied unchanged.  Keys stored in a circular
+ * cache must carry their absolute-position rotation, applied before the write [RING
+ * "proposed boundary"].
+ *  d_rope (device fp32, [rope_positions][head_dim/2][2]): (cos, sin) of the angle of pair
+ *    j at position p; pair j of a head is (x[2j], x[2j+1]) and turns to
+ *    (x0 cos - x1 sin, x0 sin + x1 cos), computed in fp32 and rounded to the store type.
+ *  Position of token i: CIRCULAR (chunks reserved - 1) * chunk + i; LINEAR the reserved
+ *    base + i, or d_slots[i] when given; PACKED i (position within its row).
+ * Tokens whose position is outside [0, rope_positions) are not written (K nor V) and
+ * set KVC_DEV_BAD_POS.  Other rules and errors as kvc_write. */
+int kvc_write_rope(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, const int32_t* d_slots,
+                   const float* d_rope, int32_t rope_positions, void* stream);
 
 /* Set lengths from device arrays (either may be NULL).
  *  d_kv_len (int32[B]): LINEAR / CIRCULAR active prefix per row [PFX "Change"; the

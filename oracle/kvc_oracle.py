@@ -216,6 +216,24 @@ class ChronoCache:
 
 
 # ---------------------------------------------------------------------------
+# RoPE at absolute positions (flashdreams issue, "proposed boundary": absolute positions
+# determine RoPE before storage)
+# ---------------------------------------------------------------------------
+def rope_apply(x, positions, table):
+    """Rotate pair j = (x[..., 2j], x[..., 2j+1]) of each token by the (cos, sin) that
+    ``table[pos, j]`` holds, in fp64.  x: ``[n, Hkv, D]``; positions: ``[n]``."""
+    x = np.asarray(x, dtype=np.float64)
+    t = np.asarray(table, dtype=np.float64)[np.asarray(positions)]      # [n, D/2, 2]
+    c = t[:, None, :, 0]
+    s = t[:, None, :, 1]
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Attention
 # ---------------------------------------------------------------------------
 def default_scale(head_dim: int) -> float:

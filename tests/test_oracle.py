@@ -369,3 +369,48 @@ def test_planted_gqa_mapping_is_caught():
                        np.repeat(v, 4, axis=1)[:, [h % 2 for h in range(8)]])
     assert np.abs(good - sdpa_ref(q, k, v)).max() < 1e-13
     assert np.abs(wrong - sdpa_ref(q, k, v)).max() > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# RoPE at absolute positions
+# ---------------------------------------------------------------------------
+def test_rope_apply_matches_independent_rotation():
+    from diffusion_serving_gb300 import workloads as wl
+    D, n = 64, 9
+    table = wl.rope_table(100, D)
+    x = torch.randn(1, n, 2, D, dtype=torch.float64)
+    pos = [0, 1, 5, 17, 33, 50, 64, 80, 99]
+    ref = wl.rope_rotate(x, pos)[0].numpy()            # computes its own fp64 cos/sin
+    got = orc.rope_apply(x[0].numpy(), pos, table.numpy())
+    assert np.abs(got - ref).max() < 1e-5              # the table is fp32-rounded
+
+
+def test_rope_apply_invariants():
+    from diffusion_serving_gb300 import workloads as wl
+    D = 128
+    table = wl.rope_table(4096, D).numpy().astype(np.float64)
+    x = rnd((6, 3, D), 90)
+    pos = [0, 1, 7, 1000, 4000, 4095]
+    y = orc.rope_apply(x, pos, table)
+    # position 0 is the identity
+    assert np.array_equal(y[0], x[0])
+    # each pair keeps its norm (cos^2 + sin^2 = 1 up to the table's fp32 rounding)
+    n_x = x[..., 0::2] ** 2 + x[..., 1::2] ** 2
+    n_y = y[..., 0::2] ** 2 + y[..., 1::2] ** 2
+    assert np.abs(n_y - n_x).max() <= 1e-6 * n_x.max()
+    # turning back by the conjugate angle restores x
+    conj = table.copy()
+    conj[..., 1] = -conj[..., 1]
+    assert np.abs(orc.rope_apply(y, pos, conj) - x).max() < 1e-6
+
+
+def test_planted_rope_sign_error_is_caught(monkeypatch):
+    real = orc.rope_apply
+
+    def wrong(x, positions, table):
+        t = np.array(table, copy=True)
+        t[..., 1] = -t[..., 1]
+        return real(x, positions, t)
+    monkeypatch.setattr(orc, "rope_apply", wrong)
+    with pytest.raises(AssertionError):
+        test_rope_apply_matches_independent_rotation()
