@@ -151,7 +151,8 @@ k_write(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* _
 // circular KV policy for streaming attention", "proposed boundary": absolute positions
 // determine RoPE before storage).  Pair j of a head, (x[2j], x[2j+1]), turns by the
 // angle whose (cos, sin) the caller's table holds at [pos][j]:
-//   (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos), fp32 FMAs, rounded to the store type.
+//   (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos), fp32 FMAs for 16-bit stores (fp64 for
+//   fp32 stores), rounded once to the store type.
 // Absolute position of token i: CIRCULAR (chunks - 1) * chunk + i; LINEAR base + i, or
 // slots[i] when slots are given; PACKED i.  Rows whose position is outside the table
 // are skipped and set KVC_DEV_BAD_POS.
@@ -180,16 +181,18 @@ template <> struct Pack<__half> {
     }
   }
 };
+// fp32 stores turn the pair in fp64 and round once, so that the stored value is the
+// correctly rounded rotation (fp32 arithmetic would leave ~1 ulp of its own rounding).
 template <> struct Pack<float> {
   static constexpr int kPairs = 2;
   __device__ static void rot(uint4& u, const float2* cs) {
     float* f = reinterpret_cast<float*>(&u);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const float x0 = f[2 * i], x1 = f[2 * i + 1];
-      const float2 c = cs[i];
-      f[2 * i] = fmaf(x0, c.x, -x1 * c.y);
-      f[2 * i + 1] = fmaf(x0, c.y, x1 * c.x);
+      const double x0 = f[2 * i], x1 = f[2 * i + 1];
+      const double c = cs[i].x, sn = cs[i].y;
+      f[2 * i] = (float)fma(x0, c, -x1 * sn);
+      f[2 * i + 1] = (float)fma(x0, sn, x1 * c);
     }
   }
 };

@@ -156,7 +156,8 @@ int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
  * "proposed boundary"].
  *  d_rope (device fp32, [rope_positions][head_dim/2][2]): (cos, sin) of the angle of pair
  *    j at position p; pair j of a head is (x[2j], x[2j+1]) and turns to
- *    (x0 cos - x1 sin, x0 sin + x1 cos), computed in fp32 and rounded to the store type.
+ *    (x0 cos - x1 sin, x0 sin + x1 cos), computed in fp32 (fp64 for an F32 store) and
+ *    rounded once to the store type.
  *  Position of token i: CIRCULAR (chunks reserved - 1) * chunk + i; LINEAR the reserved
  *    base + i, or d_slots[i] when given; PACKED i (position within its row).
  * Tokens whose position is outside [0, rope_positions) are not written (K nor V) and
