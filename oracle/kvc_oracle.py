@@ -275,6 +275,50 @@ def attend(q, k, v, scale=None, causal=False, q_pos0=0, key_pos=None):
     return out
 
 
+def attend_lse(q, k, v, scale=None, causal=False, q_pos0=0):
+    """``attend`` plus the natural-log log-sum-exp of each query row's scaled scores.
+
+    Returns (out ``[n_q, H, D]``, lse ``[n_q, H]``), fp64; a row with no visible key has
+    lse = -inf and output 0.  The pages' forward_with_lse (TensorRT-LLM PR "FA4
+    variable-length cross-attention", Microbenchmark paragraph).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    n_q, H, D = q.shape
+    n_k, Hkv, _ = k.shape
+    G = H // Hkv
+    if scale is None:
+        scale = default_scale(D)
+    out = np.zeros((n_q, H, D), dtype=np.float64)
+    lse = np.full((n_q, H), -np.inf, dtype=np.float64)
+    for h in range(H):
+        s = scale * (q[:, h, :] @ k[:, h // G, :].T)
+        if causal:
+            qp = q_pos0 + np.arange(n_q)
+            s = np.where(np.arange(n_k)[None, :] <= qp[:, None], s, -np.inf)
+        m = s.max(axis=1, keepdims=True)
+        ok = np.isfinite(m[:, 0])
+        msafe = np.where(np.isfinite(m), m, 0.0)
+        p = np.exp(s - msafe)
+        tot = p.sum(axis=1, keepdims=True)
+        out[ok, h, :] = ((p @ v[:, h // G, :]) / np.where(tot > 0, tot, 1.0))[ok]
+        lse[ok, h] = (msafe[:, 0] + np.log(np.where(tot[:, 0] > 0, tot[:, 0], 1.0)))[ok]
+    return out, lse
+
+
+def merge_lse(o_a, lse_a, o_b, lse_b):
+    """Combine two attentions over disjoint key sets from their outputs and LSEs:
+    o = (e^lse_a o_a + e^lse_b o_b) / (e^lse_a + e^lse_b), lse = log(e^lse_a + e^lse_b)."""
+    o_a, o_b = np.asarray(o_a, np.float64), np.asarray(o_b, np.float64)
+    lse_a, lse_b = np.asarray(lse_a, np.float64), np.asarray(lse_b, np.float64)
+    lse = np.logaddexp(lse_a, lse_b)
+    safe = np.where(np.isfinite(lse), lse, 0.0)
+    wa = np.where(np.isfinite(lse_a), np.exp(lse_a - safe), 0.0)[..., None]
+    wb = np.where(np.isfinite(lse_b), np.exp(lse_b - safe), 0.0)[..., None]
+    return wa * o_a + wb * o_b, lse
+
+
 def attend_masked_full(q, k_full, v_full, kv_len, scale=None):
     """Attention over a full-capacity store with the tail ``[kv_len, cap)`` masked.
 

@@ -414,3 +414,42 @@ def test_planted_rope_sign_error_is_caught(monkeypatch):
     monkeypatch.setattr(orc, "rope_apply", wrong)
     with pytest.raises(AssertionError):
         test_rope_apply_matches_independent_rotation()
+
+
+# ---------------------------------------------------------------------------
+# Log-sum-exp output and the merge of partial attentions
+# ---------------------------------------------------------------------------
+def test_lse_matches_torch_logsumexp_and_attend():
+    q, k, v = rnd((7, 4, 32), 200), rnd((50, 2, 32), 201), rnd((50, 2, 32), 202)
+    o, lse = orc.attend_lse(q, k, v)
+    assert np.abs(o - orc.attend(q, k, v)).max() < 1e-14
+    scale = 1 / math.sqrt(32)
+    for h in range(4):
+        s = torch.from_numpy(scale * (q[:, h, :] @ k[:, h // 2, :].T))
+        assert np.abs(lse[:, h] - torch.logsumexp(s, dim=1).numpy()).max() < 1e-12
+
+
+def test_lse_closed_forms():
+    q, k, v = rnd((3, 2, 16), 203), rnd((1, 2, 16), 204), rnd((1, 2, 16), 205)
+    _, lse = orc.attend_lse(q, k, v)
+    for h in range(2):
+        assert np.allclose(lse[:, h], (q[:, h, :] @ k[0, h]) / 4.0, atol=1e-14, rtol=0)
+    kk = np.broadcast_to(k, (9, 2, 16)).copy()
+    _, lse9 = orc.attend_lse(q, kk, rnd((9, 2, 16), 206))
+    assert np.allclose(lse9, lse + math.log(9), atol=1e-13, rtol=0)
+
+
+def test_merge_of_halves_equals_attention_over_union():
+    q, k, v = rnd((6, 4, 32), 210), rnd((40, 2, 32), 211), rnd((40, 2, 32), 212)
+    o, lse = orc.attend_lse(q, k, v)
+    oa, la = orc.attend_lse(q, k[:17], v[:17])
+    ob, lb = orc.attend_lse(q, k[17:], v[17:])
+    om, lm = orc.merge_lse(oa, la, ob, lb)
+    assert np.abs(om - o).max() < 1e-13 and np.abs(lm - lse).max() < 1e-13
+
+
+def test_causal_lse_of_row_without_keys():
+    q, k, v = rnd((4, 2, 8), 220), rnd((2, 2, 8), 221), rnd((2, 2, 8), 222)
+    o, lse = orc.attend_lse(q, k, v, causal=True, q_pos0=-2)       # rows 0, 1 see nothing
+    assert np.all(np.isneginf(lse[:2])) and np.all(o[:2] == 0)
+    assert np.all(np.isfinite(lse[2:]))
