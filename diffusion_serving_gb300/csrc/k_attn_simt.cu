@@ -40,7 +40,8 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 k_attn_simt(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ kst, const T* __restrict__ vst,
-            int32_t* __restrict__ meta, kvc_geom g, int n_q, int causal, float scale_log2) {
+            int32_t* __restrict__ meta, kvc_geom g, int n_q, int causal, float scale_log2,
+            float* __restrict__ lse) {
   constexpr int DL = D / 32;  // output dims per lane
   __shared__ float sK[kTile][D + 1];
   __shared__ float sV[kTile][D];
@@ -138,6 +139,8 @@ k_attn_simt(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ 
     const int i = i0 + warp * kRowsPerWarp + r;
     if (i >= n_q) continue;
     const float inv = l[r] > 0.f ? 1.f / l[r] : 0.f;
+    if (lse != nullptr && lane == 0)   // natural log of sum_j exp(scale q.k_j): m, l are in the exp2 domain
+      lse[((int64_t)b * n_q + i) * g.H + h] = l[r] > 0.f ? (m[r] + log2f(l[r])) * 0.6931471805599453f : -INFINITY;
     T* o = out + (((int64_t)b * n_q + i) * g.H + h) * D;
 #pragma unroll
     for (int t = 0; t < DL; ++t) o[lane + 32 * t] = from_f<T>(acc[r][t] * inv);
@@ -145,26 +148,27 @@ k_attn_simt(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ 
 }
 
 template <typename T>
-cudaError_t launch_t(kvc_cache* c, const void* q, void* out, int n_q, bool causal, cudaStream_t s) {
+cudaError_t launch_t(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse, cudaStream_t s) {
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
   dim3 grid((n_q + kRowsPerBlock - 1) / kRowsPerBlock, cfg.heads, cfg.batch);
   const float sl2 = c->scale * 1.4426950408889634f;
   if (cfg.head_dim == 64)
     k_attn_simt<T, 64><<<grid, kWarps * 32, 0, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta, g,
-                                                    n_q, causal ? 1 : 0, sl2);
+                                                    n_q, causal ? 1 : 0, sl2, lse);
   else
     k_attn_simt<T, 128><<<grid, kWarps * 32, 0, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta,
-                                                     g, n_q, causal ? 1 : 0, sl2);
+                                                     g, n_q, causal ? 1 : 0, sl2, lse);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal, cudaStream_t s) {
+cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
+                                 cudaStream_t s) {
   switch (c->cfg.dtype) {
-    case KVC_F32: return launch_t<float>(c, q, out, n_q, causal, s);
-    case KVC_F16: return launch_t<__half>(c, q, out, n_q, causal, s);
-    default: return launch_t<__nv_bfloat16>(c, q, out, n_q, causal, s);
+    case KVC_F32: return launch_t<float>(c, q, out, n_q, causal, lse, s);
+    case KVC_F16: return launch_t<__half>(c, q, out, n_q, causal, lse, s);
+    default: return launch_t<__nv_bfloat16>(c, q, out, n_q, causal, lse, s);
   }
 }

@@ -282,6 +282,7 @@ struct TcParams {
   int n_q;
   int causal;
   float scale_log2;
+  float* lse;        // optional [B, n_q, H] natural-log log-sum-exp of each row's scaled scores
 };
 
 // ---- the kernel --------------------------------------------------------------
@@ -521,6 +522,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool store = row < p.n_q;
+      if (p.lse != nullptr && store)   // m_ref and l are in the exp2 domain of scale * q.k
+        p.lse[((int64_t)b * p.n_q + row) * g.H + h] = l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
       uint16_t* dst = reinterpret_cast<uint16_t*>(out) + (((int64_t)b * p.n_q + row) * g.H + h) * kD;
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
@@ -580,7 +583,8 @@ bool kvc_tc_make_kv_maps(kvc_cache* c) {
   return true;
 }
 
-cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal, cudaStream_t s) {
+cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
+                               cudaStream_t s) {
   const kvc_config& cfg = c->cfg;
   CUtensorMap tm_q;
   if (!make_map(&tm_q, cfg.dtype, q, cfg.heads, (uint64_t)n_q, cfg.batch)) return cudaErrorInvalidValue;
@@ -589,6 +593,7 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
   p.n_q = n_q;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = c->scale * 1.4426950408889634f;
+  p.lse = lse;
   dim3 grid((n_q + 2 * kBM - 1) / (2 * kBM), cfg.heads, cfg.batch);
   if (cfg.dtype == KVC_BF16)
     k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, out, c->meta, p);

@@ -137,7 +137,8 @@ __host__ __device__ constexpr size_t dyn_smem_bytes() { return (size_t)kStages *
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const T* __restrict__ q,
-         T* __restrict__ out, int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2) {
+         T* __restrict__ out, int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2,
+         float* __restrict__ lse) {
   constexpr int VPL = D / 64;        // 16-byte vectors (= 64-dim boxes) per lane per row
   constexpr int EPL = VPL * 8;       // dims per lane
   constexpr uint32_t BOX = box_bytes<D>();
@@ -401,7 +402,10 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-    if (lane == 0) s_inv[gg] = 1.f / L;
+    if (lane == 0) {
+      s_inv[gg] = 1.f / L;
+      if (lse != nullptr) lse[(int64_t)b * g.H + kvh * G + gg] = (M + log2f(L)) * 0.6931471805599453f;
+    }
   }
   __syncthreads();
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
@@ -421,30 +425,31 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare) {
+cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s, bool prepare) {
   constexpr size_t smem = dyn_smem_bytes<D>();
   if (prepare) return cudaFuncSetAttribute(k_decode<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
   k_decode<T, D, G><<<grid, kThreads, smem, s>>>(c->tm_dk, c->tm_dv, (const T*)q, (T*)out, c->meta, (float*)c->ws, g,
-                                                 c->scale * 1.4426950408889634f);
+                                                 c->scale * 1.4426950408889634f, lse);
   return cudaGetLastError();
 }
 
 template <typename T, int D>
-cudaError_t launch_d(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare) {
+cudaError_t launch_d(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s, bool prepare) {
   switch (c->cfg.heads / c->cfg.kv_heads) {
-    case 1: return launch_dg<T, D, 1>(c, q, out, s, prepare);
-    case 2: return launch_dg<T, D, 2>(c, q, out, s, prepare);
-    case 4: return launch_dg<T, D, 4>(c, q, out, s, prepare);
-    default: return launch_dg<T, D, 8>(c, q, out, s, prepare);
+    case 1: return launch_dg<T, D, 1>(c, q, out, lse, s, prepare);
+    case 2: return launch_dg<T, D, 2>(c, q, out, lse, s, prepare);
+    case 4: return launch_dg<T, D, 4>(c, q, out, lse, s, prepare);
+    default: return launch_dg<T, D, 8>(c, q, out, lse, s, prepare);
   }
 }
 
 template <typename T>
-cudaError_t launch_t(kvc_cache* c, const void* q, void* out, cudaStream_t s, bool prepare) {
-  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, s, prepare) : launch_d<T, 128>(c, q, out, s, prepare);
+cudaError_t launch_t(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s, bool prepare) {
+  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, lse, s, prepare)
+                               : launch_d<T, 128>(c, q, out, lse, s, prepare);
 }
 
 // The decode kernels opt into their dynamic shared memory once per process and
@@ -462,7 +467,8 @@ cudaError_t prepare_once(kvc_cache* c) {
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lock(g_prep_mu);
   if (g_prepared[dev][ti][di][gi]) return cudaSuccess;
-  e = ti == 0 ? launch_t<__half>(c, nullptr, nullptr, 0, true) : launch_t<__nv_bfloat16>(c, nullptr, nullptr, 0, true);
+  e = ti == 0 ? launch_t<__half>(c, nullptr, nullptr, nullptr, 0, true)
+              : launch_t<__nv_bfloat16>(c, nullptr, nullptr, nullptr, 0, true);
   if (e == cudaSuccess) g_prepared[dev][ti][di][gi] = true;
   return e;
 }
@@ -490,11 +496,11 @@ bool kvc_make_decode_maps(kvc_cache* c) {
          kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile);
 }
 
-cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s) {
+cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s) {
   const cudaError_t e = prepare_once(c);
   if (e != cudaSuccess) return e;
-  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, s, false)
-                                 : launch_t<__nv_bfloat16>(c, q, out, s, false);
+  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, lse, s, false)
+                                 : launch_t<__nv_bfloat16>(c, q, out, lse, s, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -576,5 +582,5 @@ extern "C" int kvc_attend_decode_noalloc(const kvc_config* cfg, const void* k_st
   const size_t pairs = (size_t)cfg->batch * cfg->kv_heads;
   if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - pairs * 4), 0, pairs * 4, s) != cudaSuccess)
     return KVC_ERR_CUDA;
-  return kvc_launch_decode(&c, q, out, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+  return kvc_launch_decode(&c, q, out, nullptr, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }

@@ -59,6 +59,17 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int launched(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
 
+// Kernel choice by shape only: fp32 (or the SIMT flag) -> fp32-FMA kernel; one query
+// token -> split-KV decode; bf16/fp16 with D = 128 -> tensor-core kernel; otherwise the
+// fp32-FMA kernel.
+int attend_impl(kvc_cache* c, const void* q, void* out, float* lse, int n_q, bool causal, bool simt,
+                cudaStream_t s) {
+  if (simt || c->cfg.dtype == KVC_F32) return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, lse, s));
+  if (n_q == 1 && c->dec_splits > 0) return launched(kvc_launch_decode(c, q, out, lse, s));
+  if (c->tc_ok) return launched(kvc_launch_attn_tc(c, q, out, n_q, causal, lse, s));
+  return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, lse, s));
+}
+
 }  // namespace
 
 // ---- TMA descriptors ---------------------------------------------------------
@@ -214,10 +225,23 @@ int kvc_attend(kvc_cache* c, const void* q, void* out, int32_t n_q, uint32_t fla
   const bool causal = (flags & KVC_CAUSAL) != 0;
   if (causal && c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
   cudaStream_t s = as_stream(stream);
-  if ((flags & KVC_KERNEL_SIMT) || c->cfg.dtype == KVC_F32) return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, s));
-  if (n_q == 1 && c->dec_splits > 0) return launched(kvc_launch_decode(c, q, out, s));
-  if (c->tc_ok) return launched(kvc_launch_attn_tc(c, q, out, n_q, causal, s));
-  return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, s));
+  return attend_impl(c, q, out, nullptr, n_q, causal, (flags & KVC_KERNEL_SIMT) != 0, s);
+}
+
+int kvc_attend_lse(kvc_cache* c, const void* q, void* out, float* d_lse, int32_t n_q, uint32_t flags,
+                   void* stream) {
+  if (c == nullptr || !q || !out || !d_lse || !aligned16(q) || !aligned16(out) || n_q < 1) return KVC_ERR_ARG;
+  if (((uintptr_t)d_lse & 3u) != 0 || (flags & ~(uint32_t)(KVC_CAUSAL | KVC_KERNEL_SIMT))) return KVC_ERR_ARG;
+  const bool causal = (flags & KVC_CAUSAL) != 0;
+  if (causal && c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
+  return attend_impl(c, q, out, d_lse, n_q, causal, (flags & KVC_KERNEL_SIMT) != 0, as_stream(stream));
+}
+
+int kvc_merge(int32_t dtype, int32_t n_rows, int32_t head_dim, const void* o_a, const float* lse_a, const void* o_b,
+              const float* lse_b, void* out, float* lse_out, void* stream) {
+  if (dtype < KVC_F32 || dtype > KVC_BF16 || n_rows < 1 || head_dim < 1) return KVC_ERR_ARG;
+  if (!o_a || !o_b || !out || !lse_a || !lse_b) return KVC_ERR_ARG;
+  return launched(kvc_launch_merge(dtype, n_rows, head_dim, o_a, lse_a, o_b, lse_b, out, lse_out, as_stream(stream)));
 }
 
 int kvc_reset(kvc_cache* c, int32_t row, void* stream) {

@@ -86,16 +86,18 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
                              cudaStream_t s);
 cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
                                   const float* rope, int rope_positions, cudaStream_t s);
-cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
+cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
                                  cudaStream_t s);
-cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, cudaStream_t s);
+cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s);
 cudaError_t kvc_prepare_decode(kvc_cache* c);
 bool kvc_decode_supported(const kvc_config& cfg);
 int kvc_internal_check_config(const kvc_config* cfg, int* cap);
 int kvc_internal_decode_splits(const kvc_config& cfg, int cap);
 size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits);
-cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal,
+cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
                                cudaStream_t s);
+cudaError_t kvc_launch_merge(int dtype, int rows, int head_dim, const void* oa, const float* la, const void* ob,
+                             const float* lb, void* out, float* lse, cudaStream_t s);
 bool kvc_tc_supported(const kvc_config& cfg);
 bool kvc_tc_make_kv_maps(kvc_cache* c);
 // 4-D TMA map over a 16-bit tensor [d3][d2][d1][D] (D = 64 or 128), 128B-swizzled boxes

@@ -60,6 +60,8 @@ def _load():
         "kvc_write_rope": (ctypes.c_int, [P, P, P, I32, P, P, I32, P]),
         "kvc_set_lengths": (ctypes.c_int, [P, P, P, P]),
         "kvc_attend": (ctypes.c_int, [P, P, P, I32, U32, P]),
+        "kvc_attend_lse": (ctypes.c_int, [P, P, P, P, I32, U32, P]),
+        "kvc_merge": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, P, P]),
         "kvc_reset": (ctypes.c_int, [P, I32, P]),
         "kvc_get_error": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
         "kvc_destroy": (ctypes.c_int, [P]),
@@ -152,6 +154,16 @@ def kvc_attend(h: int, q, out, n_q: int, flags: int = 0, stream=None) -> None:
     _check(_lib.kvc_attend(h, _ptr(q), _ptr(out), n_q, flags, _stream(stream)), "kvc_attend")
 
 
+def kvc_attend_lse(h: int, q, out, lse, n_q: int, flags: int = 0, stream=None) -> None:
+    _check(_lib.kvc_attend_lse(h, _ptr(q), _ptr(out), _ptr(lse), n_q, flags, _stream(stream)), "kvc_attend_lse")
+
+
+def kvc_merge(dtype, n_rows: int, head_dim: int, o_a, lse_a, o_b, lse_b, out, lse_out=None, stream=None) -> None:
+    d = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    _check(_lib.kvc_merge(d, n_rows, head_dim, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(out),
+                          _ptr(lse_out), _stream(stream)), "kvc_merge")
+
+
 def kvc_reset(h: int, row: int = -1, stream=None) -> None:
     _check(_lib.kvc_reset(h, row, _stream(stream)), "kvc_reset")
 
@@ -221,6 +233,14 @@ class KVCache:
             out = torch.empty_like(q)
         kvc_attend(self.handle, q, out, q.shape[1], flags, stream)
         return out
+
+    def attend_lse(self, q, out=None, flags=0, stream=None):
+        """(out, lse) with lse [B, n_q, H] fp32."""
+        if out is None:
+            out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+        kvc_attend_lse(self.handle, q, out, lse, q.shape[1], flags, stream)
+        return out, lse
 
     def reset(self, row=-1, stream=None):
         kvc_reset(self.handle, row, stream)

@@ -187,6 +187,22 @@ int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_s
 int kvc_attend(kvc_cache* c, const void* q, void* out, int32_t n_q, uint32_t flags,
                void* stream);
 
+/* kvc_attend that also writes the log-sum-exp of every query row's scaled scores:
+ * d_lse[b, i, h] = ln(sum_j exp(scale * q[b,i,h,:] . k_j)) over the same slots (device
+ * fp32 [B, n_q, H]; -inf for a row that sees no slot).  The forward_with_lse of [VAR];
+ * with kvc_merge it composes attentions over disjoint key sets (a cache split across
+ * stores, or a window not made of whole chunks).  Arguments and errors as kvc_attend. */
+int kvc_attend_lse(kvc_cache* c, const void* q, void* out, float* d_lse, int32_t n_q, uint32_t flags,
+                   void* stream);
+
+/* Merge two attention results over disjoint key sets, row by row (device buffers):
+ *   L = ln(e^lse_a + e^lse_b),  out = e^(lse_a - L) o_a + e^(lse_b - L) o_b.
+ * o_a, o_b, out: [n_rows, head_dim] of `dtype` (kvc_dtype); lse_a, lse_b: fp32 [n_rows];
+ * lse_out: fp32 [n_rows] or NULL.  out may alias o_a or o_b.  A row with both lse = -inf
+ * gets out = 0 and L = -inf.  Errors: KVC_ERR_ARG, KVC_ERR_CUDA. */
+int kvc_merge(int32_t dtype, int32_t n_rows, int32_t head_dim, const void* o_a, const float* lse_a,
+              const void* o_b, const float* lse_b, void* out, float* lse_out, void* stream);
+
 /* Forget the contents of `row` (all rows when row < 0): no chunk reserved, nothing
  * filled, kv_len 0; storage bytes are left as they are [RING "proposed boundary"
  * reset semantics]. */

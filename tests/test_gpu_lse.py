@@ -1,0 +1,103 @@
+"""GPU tests of attention with log-sum-exp output and of the two-way merge.
+
+The LSE of each row (ln sum_j exp(scale q.k_j)) lets attentions over disjoint key sets
+be combined exactly (the forward_with_lse of the TensorRT-LLM PR "FA4 variable-length
+cross-attention").  Checked for every kernel against the oracle, and by splitting one
+store's keys into two stores and merging.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kvc_oracle as orc
+from tests.helpers import assert_close, to64
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from diffusion_serving_gb300 import kvc
+
+LSE_ATOL = 2e-3
+
+
+def filled_linear(B, H, Hkv, D, dtype, cap, lens, seed):
+    c = kvc.KVCache(B, H, Hkv, D, dtype, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    c.k_store.normal_(generator=g)
+    c.v_store.normal_(generator=g)
+    c.set_lengths(kv_len=torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    return c, g
+
+
+@pytest.mark.parametrize("dtype,n_q,flags,H,Hkv", [
+    (torch.bfloat16, 300, 0, 4, 4),          # tensor-core kernel
+    (torch.float16, 1, 0, 8, 2),             # split-KV decode
+    (torch.float32, 37, 0, 2, 2),            # fp32-FMA kernel
+    (torch.bfloat16, 40, 256, 4, 2),         # fp32-FMA kernel forced on bf16
+])
+def test_attend_lse_matches_oracle(dtype, n_q, flags, H, Hkv):
+    B, D, cap = 2, 128, 3000
+    lens = [2049, 130]
+    c, g = filled_linear(B, H, Hkv, D, dtype, cap, lens, n_q + H)
+    q = torch.randn(B, n_q, H, D, device="cuda", generator=g).to(dtype)
+    out, lse = c.attend_lse(q, flags=flags)
+    plain = c.attend(q, flags=flags)
+    assert torch.equal(out, plain)                      # the LSE costs nothing in the output
+    for b in range(B):
+        ref_o, ref_l = orc.attend_lse(to64(q[b]), to64(c.k_store[b, :lens[b]]), to64(c.v_store[b, :lens[b]]))
+        assert_close(out[b], ref_o, f"row {b}")
+        assert np.abs(lse[b].cpu().double().numpy() - ref_l).max() < LSE_ATOL
+    assert c.get_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_split_then_merge_equals_whole(dtype):
+    """Keys split across two stores, attended separately, merged: equal to one store."""
+    B, H, D, n_q = 1, 4, 128, 200
+    n_a, n_b = 700, 333
+    g = torch.Generator(device="cuda").manual_seed(9)
+    k = torch.randn(B, n_a + n_b, H, D, device="cuda", generator=g).to(dtype)
+    v = torch.randn(B, n_a + n_b, H, D, device="cuda", generator=g).to(dtype)
+    q = torch.randn(B, n_q, H, D, device="cuda", generator=g).to(dtype)
+    whole = kvc.KVCache(B, H, H, D, dtype, "linear", capacity=n_a + n_b)
+    whole.advance(n_tokens=n_a + n_b)
+    whole.write(k, v)
+    part_a = kvc.KVCache(B, H, H, D, dtype, "linear", capacity=n_a)
+    part_a.advance(n_tokens=n_a)
+    part_a.write(k[:, :n_a].contiguous(), v[:, :n_a].contiguous())
+    part_b = kvc.KVCache(B, H, H, D, dtype, "linear", capacity=n_b)
+    part_b.advance(n_tokens=n_b)
+    part_b.write(k[:, n_a:].contiguous(), v[:, n_a:].contiguous())
+    o_w, l_w = whole.attend_lse(q)
+    o_a, l_a = part_a.attend_lse(q)
+    o_b, l_b = part_b.attend_lse(q)
+    merged = torch.empty_like(o_a)
+    l_m = torch.empty_like(l_a)
+    rows = B * n_q * H
+    kvc.kvc_merge(dtype, rows, D, o_a, l_a, o_b, l_b, merged, l_m)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.attend_lse(to64(q[0]), to64(k[0]), to64(v[0]))
+    assert_close(merged[0], ref_o, "merged vs oracle")
+    assert np.abs(l_m[0].cpu().double().numpy() - ref_l).max() < LSE_ATOL
+    # the merged result agrees with the one-store attention within rounding of the halves
+    assert (merged.float() - o_w.float()).abs().max().item() < 1e-2
+    assert (l_m - l_w).abs().max().item() < LSE_ATOL
+
+
+def test_merge_rows_without_keys():
+    rows, D = 64, 128
+    oa = torch.randn(rows, D, device="cuda").bfloat16()
+    ob = torch.randn(rows, D, device="cuda").bfloat16()
+    la = torch.randn(rows, device="cuda")
+    lb = torch.randn(rows, device="cuda")
+    la[:8] = float("-inf")                               # half a: no key for rows 0-7
+    lb[:4] = float("-inf")                               # rows 0-3: no key at all
+    out = torch.empty_like(oa)
+    lo = torch.empty_like(la)
+    kvc.kvc_merge(torch.bfloat16, rows, D, oa, la, ob, lb, out, lo)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.merge_lse(to64(oa), la.double().cpu().numpy(), to64(ob), lb.double().cpu().numpy())
+    assert torch.all(out[:4] == 0) and torch.all(torch.isneginf(lo[:4]))
+    assert np.abs(to64(out) - ref_o).max() < 1e-2
+    fin = np.isfinite(ref_l)
+    assert np.abs(lo.double().cpu().numpy()[fin] - ref_l[fin]).max() < 1e-5
