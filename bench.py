@@ -142,14 +142,15 @@ class Clocks:
 def ring_flops(w):
     """Algorithmic flops of one step (every chunk, every rewrite, valid slots only)."""
     total = 0.0
-    per_attend = []
+    per_attend, per_kv = [], []
     for c in range(w.n_chunks):
         kv = min((c + 1) * w.chunk, w.window)
         f = wl.attention_flops(w.chunk, kv, w.heads, w.head_dim) * w.batch
         for _ in range(w.rewrites):
             per_attend.append(f)
+            per_kv.append(kv)
             total += f
-    return total, per_attend
+    return total, per_attend, per_kv
 
 
 def make_inputs(w, device, pool):
@@ -238,6 +239,25 @@ def decode_bench(kvc, peaks, per_graph=64, replays=5):
     return res
 
 
+def tc_traffic_per_launch(w, per_attend_kv):
+    """DRAM bytes per attend launch, from the committed capture of the chunk kernel:
+    the capture's DRAM / algorithmic ratio times this workload's average algorithmic
+    bytes (Q and O once, valid K/V once).  None when the kernel source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "k_attn_tc_traffic.json")
+    src = os.path.join(ROOT, "diffusion_serving_gb300", "csrc", "k_attn_tc.cu")
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    with open(path) as f:
+        cap = json.load(f)
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != cap["kernel_source_sha256"]:
+            return None
+    qo = 2 * w.batch * w.chunk * w.heads * w.head_dim * 2
+    kv = [2 * w.batch * n * w.kv_heads * w.head_dim * 2 for n in per_attend_kv]
+    return round(cap["dram_over_algorithmic"] * (qo + float(np.mean(kv))))
+
+
 def cpu_oracle_sample(w, budget_s=12.0):
     """Time the fp64 oracle on sampled query rows of a full-window attend."""
     from oracle import kvc_oracle as orc
@@ -285,7 +305,7 @@ def ours(args):
                         chunk=w.chunk)
     inputs = make_inputs(w, "cuda", pool=min(args.pool, w.n_chunks * w.rewrites))
     out = torch.empty_like(inputs[0][0])
-    step_flops, per_attend = ring_flops(w)
+    step_flops, per_attend, per_kv = ring_flops(w)
 
     for _ in range(args.warmup):
         run_step(cache, w, inputs, out, stream)
@@ -340,12 +360,32 @@ def ours(args):
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": launches,
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peaks["bf16_sust"],
-                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_sust"], 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_sust"], 4),
+                     "traffic": tc_traffic_per_launch(w, per_kv),
+                     "traffic_note": "bytes per average launch, scaled from profiles/k_attn_tc_traffic.json",
                      "kernel": "chunk attention (attend)", "peak_kind": f"bf16 dense sustained, {peaks['src']}",
                      "attend_ms_avg": round(avg_attend_t * 1e3, 3)},
         "write": {"GB/s": round(write_gbs, 1), "frac": round(write_gbs / peaks["hbm"], 4),
                   "bytes_per_launch": write_bytes, "us_avg": round(float(np.mean(write_t)) * 1e6, 2)},
     }
+    # the per-step copy a chronological store would make (the circular layout skips it)
+    scratch = torch.empty(kvc.kvc_roll_scratch_bytes(cache.cfg), dtype=torch.uint8, device="cuda")
+    if scratch.numel() > 0:
+        kvc.kvc_roll_window(cache.handle, scratch)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        a.record()
+        for _ in range(reps):
+            kvc.kvc_roll_window(cache.handle, scratch)
+        b.record()
+        b.synchronize()
+        roll_t = a.elapsed_time(b) * 1e-3 / reps
+        roll_bytes = 8 * w.batch * (w.window - w.sink - w.chunk) * row_bytes
+        result["roll_comparator"] = {"us": round(roll_t * 1e6, 1), "GB/s": round(roll_bytes / roll_t / 1e9, 1),
+                                     "bytes": roll_bytes, "x_write": round(roll_t / float(np.mean(write_t)), 2),
+                                     "note": "clone + copy-back of the retained window, per chunk step; "
+                                             "the circular layout does not do it"}
+        del scratch
     clocks = clk.summary()
     if clocks is not None:
         result["clocks"] = clocks

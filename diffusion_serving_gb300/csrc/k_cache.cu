@@ -257,6 +257,38 @@ k_write_rope(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uin
   }
 }
 
+// Comparator for measurement, not on the path: the copy a chronological sink + window
+// store makes once per chunk step (flashdreams issue "add an opt-in circular KV policy
+// for streaming attention", "current path": the retained keys and values are cloned and
+// copied back one chunk to the left).  Rows [first, first + count) of every batch row
+// move between `src` (row stride src_cap) and `dst` (row stride dst_cap), K and V in
+// one launch; the roll is two such launches: store -> scratch, scratch -> store.
+__global__ void __launch_bounds__(kWriteThreads)
+k_copy_rows(const uint4* __restrict__ ks, const uint4* __restrict__ vs, uint4* __restrict__ kd,
+            uint4* __restrict__ vd, int B, int count, int src_cap, int src_first, int dst_cap, int dst_first,
+            int row_vecs) {
+  const int lane = threadIdx.x & 31;
+  const int rows_per_tensor = B * count;
+  const int rows = 2 * rows_per_tensor;
+  const int warps = (gridDim.x * blockDim.x) >> 5;
+  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+    const int t = r >= rows_per_tensor;
+    const int e = r - (t ? rows_per_tensor : 0);
+    const int b = e / count, i = e - b * count;
+    const uint4* src = (t ? vs : ks) + ((int64_t)b * src_cap + src_first + i) * row_vecs;
+    uint4* dst = (t ? vd : kd) + ((int64_t)b * dst_cap + dst_first + i) * row_vecs;
+    for (int v0 = lane; v0 < row_vecs; v0 += 32 * kWriteUnroll) {
+      uint4 val[kWriteUnroll];
+#pragma unroll
+      for (int u = 0; u < kWriteUnroll; ++u)
+        if (v0 + 32 * u < row_vecs) val[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kWriteUnroll; ++u)
+        if (v0 + 32 * u < row_vecs) dst[v0 + 32 * u] = val[u];
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t kvc_launch_advance(kvc_cache* c, int row, int n, cudaStream_t s) {
@@ -306,5 +338,25 @@ cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, in
   else if (g.dtype == KVC_F16) KVC_WR(__half);
   else KVC_WR(__nv_bfloat16);
 #undef KVC_WR
+  return cudaGetLastError();
+}
+
+cudaError_t kvc_launch_roll(kvc_cache* c, void* scratch, cudaStream_t s) {
+  const kvc_config& g = c->cfg;
+  const int row_vecs = g.kv_heads * g.head_dim * c->eb / 16;
+  const int count = g.window - g.sink - g.chunk;         // retained rolling tokens
+  if (count <= 0) return cudaSuccess;
+  const int64_t rows = 2LL * g.batch * count;
+  int64_t blocks = (rows + kWriteThreads / 32 - 1) / (kWriteThreads / 32);
+  const int64_t max_blocks = (int64_t)c->num_sms * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  uint4* sk = static_cast<uint4*>(scratch);
+  uint4* sv = sk + (int64_t)g.batch * count * row_vecs;
+  // clone: store rows [sink + chunk, window) -> scratch
+  k_copy_rows<<<(unsigned)blocks, kWriteThreads, 0, s>>>((const uint4*)c->k, (const uint4*)c->v, sk, sv, g.batch,
+                                                         count, c->cap, g.sink + g.chunk, count, 0, row_vecs);
+  // copy back one chunk to the left: scratch -> store rows [sink, window - chunk)
+  k_copy_rows<<<(unsigned)blocks, kWriteThreads, 0, s>>>(sk, sv, (uint4*)c->k, (uint4*)c->v, g.batch, count, count,
+                                                         0, c->cap, g.sink, row_vecs);
   return cudaGetLastError();
 }

@@ -10,8 +10,8 @@
 // of the row's kv_len slots; the share is computed on the device from kv_len, so the
 // grid depends only on the shape and a captured graph replays at any length.
 // A producer warp streams the share through a ring of shared-memory stages with TMA
-// tile loads (112 slots x 64 dims per box, 128-byte swizzle): one instruction moves
-// 14 KB, so the whole stream needs a few hundred copy requests per SM.  Seven consumer
+// tile loads (112 whole rows of one kv head per box): one instruction moves 28 KB of K
+// or V, so the whole stream needs a few hundred copy requests per SM.  Seven consumer
 // warps take 16 slots of every 112-slot tile each, as 4 independent row groups whose
 // loads and dot products overlap and keep an online softmax (running
 // max m, sum l, accumulator) per q head; their states merge in shared memory into one
@@ -20,8 +20,8 @@
 // next call) merges the partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 //
 // Lane mapping: 8 lanes per slot row, 4 rows per warp instruction; lane sub holds dims
-// {64 v + 8 sub + i : v < D/64, i < 8}, i.e. 16-byte chunk `sub` of each 64-dim box, so
-// the 8 lanes of a row read one whole 128-byte swizzled row (conflict-free).
+// {64 v + 8 sub + i : v < D/64, i < 8}, i.e. 16-byte chunk `sub` of each 64-dim half, so
+// the 8 lanes of a row read 128 contiguous bytes per load (one wavefront per row).
 #include "kvc_internal.h"
 
 #include <cuda_bf16.h>
@@ -128,9 +128,9 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 template <int D>
-__host__ __device__ constexpr uint32_t box_bytes() { return kTile * 128u; }           // kTile slots x 64 dims x 2 B
+__host__ __device__ constexpr uint32_t box_bytes() { return kTile * D * 2u; }         // kTile whole rows
 template <int D>
-__host__ __device__ constexpr uint32_t stage_bytes() { return 2u * (D / 64) * box_bytes<D>(); }   // K and V
+__host__ __device__ constexpr uint32_t stage_bytes() { return 2u * box_bytes<D>(); }  // K and V
 template <int D>
 __host__ __device__ constexpr size_t dyn_smem_bytes() { return (size_t)kStages * stage_bytes<D>() + 1024; }
 
@@ -187,11 +187,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         mbar_expect_tx(&full[st], SB);
         uint8_t* dst = dsm + st * SB;
         const int row = row0 + t0 + t * kTile;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-          tma_load_4d(&tm_k, &full[st], dst + v * BOX, v * 64, kvh, row, kv_batch);
-          tma_load_4d(&tm_v, &full[st], dst + (VPL + v) * BOX, v * 64, kvh, row, kv_batch);
-        }
+        tma_load_4d(&tm_k, &full[st], dst, 0, kvh, row, kv_batch);
+        tma_load_4d(&tm_v, &full[st], dst + BOX, 0, kvh, row, kv_batch);
         issued = t + 1;
       }
       if (*abort) {   // let every load issued here land before the block releases its shared memory
@@ -225,7 +222,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
       const int st = t % kStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (t / kStages) & 1, abort))) break;
       const uint8_t* kst = dsm + st * SB;
-      const uint8_t* vst = kst + VPL * BOX;
+      const uint8_t* vst = kst + BOX;
       const int first = t * kTile + warp * kRowsPerWarp;   // this warp's rows of the tile
       if (first < nt) {
         // scores of the warp's kGroups row groups (independent: they overlap in flight)
@@ -233,11 +230,11 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
         for (int u = 0; u < kGroups; ++u) {
           const int r = warp * kRowsPerWarp + u * 4 + grp;          // row within the tile
-          const uint32_t off = r * 128 + ((sub ^ (r & 7)) << 4);     // 128B swizzle: chunk `sub` of row r
+          const uint32_t off = r * (D * 2) + sub * 16;                // 16-byte chunk `sub` of each 64-dim half
           float kf[EPL];
 #pragma unroll
           for (int v = 0; v < VPL; ++v)
-            unpack8(*reinterpret_cast<const uint4*>(kst + v * BOX + off), &kf[8 * v], (const T*)nullptr);
+            unpack8(*reinterpret_cast<const uint4*>(kst + off + v * 128), &kf[8 * v], (const T*)nullptr);
 #pragma unroll
           for (int gg = 0; gg < G; ++gg) {
             float2 a2 = make_float2(0.f, 0.f);
@@ -287,11 +284,11 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
         for (int u = 0; u < kGroups; ++u) {
           const int r = warp * kRowsPerWarp + u * 4 + grp;
-          const uint32_t off = r * 128 + ((sub ^ (r & 7)) << 4);
+          const uint32_t off = r * (D * 2) + sub * 16;
           float vf[EPL];
 #pragma unroll
           for (int v = 0; v < VPL; ++v)
-            unpack8(*reinterpret_cast<const uint4*>(vst + v * BOX + off), &vf[8 * v], (const T*)nullptr);
+            unpack8(*reinterpret_cast<const uint4*>(vst + off + v * 128), &vf[8 * v], (const T*)nullptr);
           if (partial && first + u * 4 + grp >= nt) {
 #pragma unroll
             for (int e = 0; e < EPL; ++e) vf[e] = 0.f;
@@ -492,8 +489,8 @@ cudaError_t kvc_prepare_decode(kvc_cache* c) { return prepare_once(c); }
 bool kvc_make_decode_maps(kvc_cache* c) {
   const kvc_config& g = c->cfg;
   const uint64_t batches = g.layout == KVC_PACKED ? 1 : (uint64_t)g.batch;
-  return kvc_make_tile_map(&c->tm_dk, g.dtype, c->k, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile) &&
-         kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile);
+  return kvc_make_tile_map(&c->tm_dk, g.dtype, c->k, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile, true) &&
+         kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile, true);
 }
 
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s) {

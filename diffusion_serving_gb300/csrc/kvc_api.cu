@@ -93,16 +93,16 @@ EncodeTiledFn encode_fn() {
 }  // namespace
 
 bool kvc_make_tile_map(CUtensorMap* m, int dtype, const void* base, int D, uint64_t d1, uint64_t d2, uint64_t d3,
-                       uint32_t box_rows) {
+                       uint32_t box_rows, bool whole_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr || (dtype != KVC_BF16 && dtype != KVC_F16)) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, d1, d2, d3};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2ull, d1 * D * 2ull, d2 * d1 * D * 2ull};
-  const cuuint32_t box[4] = {64, 1, box_rows, 1};
+  const cuuint32_t box[4] = {whole_rows ? (cuuint32_t)D : 64u, 1, box_rows, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUtensorMapDataType t = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return enc(m, t, 4, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             whole_rows ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -242,6 +242,21 @@ int kvc_merge(int32_t dtype, int32_t n_rows, int32_t head_dim, const void* o_a, 
   if (dtype < KVC_F32 || dtype > KVC_BF16 || n_rows < 1 || head_dim < 1) return KVC_ERR_ARG;
   if (!o_a || !o_b || !out || !lse_a || !lse_b) return KVC_ERR_ARG;
   return launched(kvc_launch_merge(dtype, n_rows, head_dim, o_a, lse_a, o_b, lse_b, out, lse_out, as_stream(stream)));
+}
+
+size_t kvc_roll_scratch_bytes(const kvc_config* cfg) {
+  int cap = 0;
+  if (check_cfg(cfg, &cap) != KVC_OK || cfg->layout != KVC_CIRCULAR) return 0;
+  const int64_t count = cfg->window - cfg->sink - cfg->chunk;
+  if (count <= 0) return 0;
+  return (size_t)2 * cfg->batch * count * cfg->kv_heads * cfg->head_dim * elem_bytes(cfg->dtype);
+}
+
+int kvc_roll_window(kvc_cache* c, void* d_scratch, void* stream) {
+  if (c == nullptr) return KVC_ERR_ARG;
+  if (c->cfg.layout != KVC_CIRCULAR) return KVC_ERR_UNSUPPORTED;
+  if (kvc_roll_scratch_bytes(&c->cfg) > 0 && (d_scratch == nullptr || !aligned16(d_scratch))) return KVC_ERR_ARG;
+  return launched(kvc_launch_roll(c, d_scratch, as_stream(stream)));
 }
 
 int kvc_reset(kvc_cache* c, int32_t row, void* stream) {

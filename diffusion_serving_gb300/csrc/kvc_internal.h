@@ -86,6 +86,7 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
                              cudaStream_t s);
 cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
                                   const float* rope, int rope_positions, cudaStream_t s);
+cudaError_t kvc_launch_roll(kvc_cache* c, void* scratch, cudaStream_t s);
 cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
                                  cudaStream_t s);
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s);
@@ -100,10 +101,10 @@ cudaError_t kvc_launch_merge(int dtype, int rows, int head_dim, const void* oa, 
                              const float* lb, void* out, float* lse, cudaStream_t s);
 bool kvc_tc_supported(const kvc_config& cfg);
 bool kvc_tc_make_kv_maps(kvc_cache* c);
-// 4-D TMA map over a 16-bit tensor [d3][d2][d1][D] (D = 64 or 128), 128B-swizzled boxes
-// of 64 x 1 x box_rows x 1 elements.  False if the driver entry point is missing or the
-// encoding is rejected.
+// 4-D TMA map over a 16-bit tensor [d3][d2][d1][D] (D = 64 or 128): 128B-swizzled boxes
+// of 64 x 1 x box_rows x 1 elements, or (whole_rows) unswizzled boxes of D x 1 x box_rows
+// x 1.  False if the driver entry point is missing or the encoding is rejected.
 bool kvc_make_tile_map(CUtensorMap* m, int dtype, const void* base, int D, uint64_t d1, uint64_t d2, uint64_t d3,
-                       uint32_t box_rows);
+                       uint32_t box_rows, bool whole_rows = false);
 // Decode maps of a store (tm_dk, tm_dv) for the config in c.
 bool kvc_make_decode_maps(kvc_cache* c);

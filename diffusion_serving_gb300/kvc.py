@@ -62,6 +62,8 @@ def _load():
         "kvc_attend": (ctypes.c_int, [P, P, P, I32, U32, P]),
         "kvc_attend_lse": (ctypes.c_int, [P, P, P, P, I32, U32, P]),
         "kvc_merge": (ctypes.c_int, [I32, I32, I32, P, P, P, P, P, P, P]),
+        "kvc_roll_scratch_bytes": (SZ, [cfgp]),
+        "kvc_roll_window": (ctypes.c_int, [P, P, P]),
         "kvc_reset": (ctypes.c_int, [P, I32, P]),
         "kvc_get_error": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
         "kvc_destroy": (ctypes.c_int, [P]),
@@ -162,6 +164,14 @@ def kvc_merge(dtype, n_rows: int, head_dim: int, o_a, lse_a, o_b, lse_b, out, ls
     d = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     _check(_lib.kvc_merge(d, n_rows, head_dim, _ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(out),
                           _ptr(lse_out), _stream(stream)), "kvc_merge")
+
+
+def kvc_roll_scratch_bytes(cfg: kvc_config) -> int:
+    return _lib.kvc_roll_scratch_bytes(ctypes.byref(cfg))
+
+
+def kvc_roll_window(h: int, scratch, stream=None) -> None:
+    _check(_lib.kvc_roll_window(h, _ptr(scratch), _stream(stream)), "kvc_roll_window")
 
 
 def kvc_reset(h: int, row: int = -1, stream=None) -> None:

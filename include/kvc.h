@@ -203,6 +203,16 @@ int kvc_attend_lse(kvc_cache* c, const void* q, void* out, float* d_lse, int32_t
 int kvc_merge(int32_t dtype, int32_t n_rows, int32_t head_dim, const void* o_a, const float* lse_a,
               const void* o_b, const float* lse_b, void* out, float* lse_out, void* stream);
 
+/* Comparator for measurement, not part of the path: the per-chunk copy that a
+ * chronological sink + window store makes and the circular layout avoids [RING "current
+ * path": the retained keys and values are cloned and copied back once per step].  On a
+ * CIRCULAR handle's store read chronologically, K and V slots [sink + chunk, window) of
+ * every row move to [sink, window - chunk) through d_scratch (clone, then copy back).
+ * d_scratch: device, kvc_roll_scratch_bytes(cfg) bytes, 16-byte aligned.
+ * Errors: KVC_ERR_UNSUPPORTED for other layouts, KVC_ERR_ARG, KVC_ERR_CUDA. */
+size_t kvc_roll_scratch_bytes(const kvc_config* cfg);
+int kvc_roll_window(kvc_cache* c, void* d_scratch, void* stream);
+
 /* Forget the contents of `row` (all rows when row < 0): no chunk reserved, nothing
  * filled, kv_len 0; storage bytes are left as they are [RING "proposed boundary"
  * reset semantics]. */

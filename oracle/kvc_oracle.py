@@ -69,6 +69,15 @@ def ring_attended(end: int, sink: int, window: int) -> list[int]:
     return head + list(range(tail_start, end))
 
 
+def roll_left(store, sink: int, window: int, chunk: int):
+    """The chronological store's per-step copy: rows ``[sink + chunk, window)`` of each
+    batch row move to ``[sink, window - chunk)`` (flashdreams issue, "current path");
+    the rest is unchanged.  ``store``: ``[B, window, ...]``."""
+    out = np.array(store, copy=True)
+    out[:, sink:window - chunk] = np.asarray(store)[:, sink + chunk:window]
+    return out
+
+
 def check_ring_layout(sink: int, window: int, chunk: int) -> None:
     """Whole-chunk sink and window sizes, as the circular policy starts with."""
     if chunk <= 0 or window <= sink or sink < 0:

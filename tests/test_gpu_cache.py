@@ -198,3 +198,21 @@ def test_graph_replay_writes_the_device_slot():
     assert torch.equal(bits(cache.v_store), bits(eager.v_store))
     assert bases == [8, 16, 24, 32, 8, 16, 24, 32]
     assert cache.get_error() == 0 and eager.get_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_roll_comparator_matches_chronological_copy(dtype):
+    """The comparator copy (what the circular layout avoids) moves the retained rolling
+    tokens one chunk to the left, bit for bit."""
+    B, Hkv, D, C, S, W = 3, 2, 64, 4, 8, 40
+    cache = kvc.KVCache(B, Hkv, Hkv, D, dtype, "circular", sink=S, window=W, chunk=C)
+    cache.k_store.normal_()
+    cache.v_store.normal_()
+    before_k, before_v = cache.k_store.cpu(), cache.v_store.cpu()
+    scratch = torch.empty(kvc.kvc_roll_scratch_bytes(cache.cfg), dtype=torch.uint8, device="cuda")
+    kvc.kvc_roll_window(cache.handle, scratch)
+    torch.cuda.synchronize()
+    want_k = orc.roll_left(bits(before_k).numpy(), S, W, C)
+    want_v = orc.roll_left(bits(before_v).numpy(), S, W, C)
+    assert np.array_equal(bits(cache.k_store.cpu()).numpy(), want_k)
+    assert np.array_equal(bits(cache.v_store.cpu()).numpy(), want_v)

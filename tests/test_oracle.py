@@ -453,3 +453,18 @@ def test_causal_lse_of_row_without_keys():
     o, lse = orc.attend_lse(q, k, v, causal=True, q_pos0=-2)       # rows 0, 1 see nothing
     assert np.all(np.isneginf(lse[:2])) and np.all(o[:2] == 0)
     assert np.all(np.isfinite(lse[2:]))
+
+
+def test_roll_left_matches_brute_force_deque():
+    """The chronological store after a roll holds the sink, then the retained tokens in
+    order (a deque that drops its oldest rolling chunk)."""
+    S, W, C = 2, 10, 2
+    store = np.arange(3 * W).reshape(3, W)
+    out = orc.roll_left(store, S, W, C)
+    for b in range(3):
+        rolling = collections.deque(store[b, S:W].tolist())
+        for _ in range(C):
+            rolling.popleft()
+        assert out[b, :S].tolist() == store[b, :S].tolist()
+        assert out[b, S:W - C].tolist() == list(rolling)
+        assert out[b, W - C:].tolist() == store[b, W - C:].tolist()
