@@ -234,6 +234,32 @@ def decode_bench(kvc, peaks, per_graph=64, replays=5):
         res[name] = {"kv_len": n, "us": round(t * 1e6, 3), "GB/s": round(nbytes / t / 1e9, 1),
                      "frac": round(nbytes / t / 1e9 / peaks["hbm"], 4), "bytes": nbytes,
                      "timing": f"graph of {per_graph} attends x {replays} replays"}
+    # whole decode step (reserve one slot, write its K/V, attend), 64 steps per graph,
+    # from a 234-token prompt: kv_len runs 235 .. 618 over the timed replays
+    c = caches[0]
+    c.reset()
+    kp = torch.randn(1, wl.DECODE_PROMPT, w.kv_heads, w.head_dim, device="cuda", generator=g).half()
+    k1 = torch.randn(1, 1, w.kv_heads, w.head_dim, device="cuda", generator=g).half()
+    c.advance(n_tokens=wl.DECODE_PROMPT)
+    c.write(kp, kp)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side):
+        for r in range(per_graph):
+            c.advance(n_tokens=1, stream=side)
+            c.write(k1, k1, stream=side)
+            c.attend(q, out, stream=side)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(replays):
+        graph.replay()
+    b.record()
+    b.synchronize()
+    t = a.elapsed_time(b) * 1e-3 / (replays * per_graph)
+    res["step_advance_write_attend"] = {"kv_len": f"{wl.DECODE_PROMPT + 1}..{wl.DECODE_PROMPT + replays * per_graph}",
+                                        "us": round(t * 1e6, 3), "tokens_per_s": round(1.0 / t, 1),
+                                        "timing": f"graph of {per_graph} steps x {replays} replays"}
     for c in caches:
         assert c.get_error() == 0
     return res

@@ -20,6 +20,8 @@ namespace {
 
 __global__ void k_advance(int32_t* __restrict__ meta, int B, int row, int n, int layout, int sink,
                           int window, int chunk, int cap) {
+  kvc_pdl_wait();
+  kvc_pdl_release();
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     if (row >= 0 && b != row) continue;
     int32_t* r = meta + kvc_meta_row(b);
@@ -54,6 +56,8 @@ __global__ void k_advance(int32_t* __restrict__ meta, int B, int row, int n, int
 }
 
 __global__ void k_reset(int32_t* __restrict__ meta, int B, int row) {
+  kvc_pdl_wait();
+  kvc_pdl_release();
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     if (row >= 0 && b != row) continue;
     int32_t* r = meta + kvc_meta_row(b);
@@ -67,6 +71,8 @@ __global__ void k_reset(int32_t* __restrict__ meta, int B, int row) {
 __global__ void k_set_lengths(int32_t* __restrict__ meta, int B, int cap, const int32_t* __restrict__ kv_len,
                               const int32_t* __restrict__ cu) {
   __shared__ int ok;
+  kvc_pdl_wait();
+  kvc_pdl_release();
   if (kv_len != nullptr) {
     for (int b = threadIdx.x; b < B; b += blockDim.x) {
       const int n = kv_len[b];
@@ -101,6 +107,8 @@ __global__ void __launch_bounds__(kWriteThreads)
 k_write(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* __restrict__ kdst,
         uint4* __restrict__ vdst, int32_t* __restrict__ meta, const int32_t* __restrict__ slots, int B, int n,
         int row_vecs, int cap, int layout) {
+  kvc_pdl_wait();
+  kvc_pdl_release();
   const int lane = threadIdx.x & 31;
   const int rows_per_tensor = B * n;
   const int rows = 2 * rows_per_tensor;
@@ -293,18 +301,16 @@ k_copy_rows(const uint4* __restrict__ ks, const uint4* __restrict__ vs, uint4* _
 
 cudaError_t kvc_launch_advance(kvc_cache* c, int row, int n, cudaStream_t s) {
   const kvc_config& g = c->cfg;
-  k_advance<<<1, 128, 0, s>>>(c->meta, g.batch, row, n, g.layout, g.sink, g.window, g.chunk, c->cap);
-  return cudaGetLastError();
+  return kvc_launch_pdl(k_advance, dim3(1), dim3(128), 0, s, c->meta, g.batch, row, n, g.layout, g.sink, g.window,
+                        g.chunk, c->cap);
 }
 
 cudaError_t kvc_launch_reset(kvc_cache* c, int row, cudaStream_t s) {
-  k_reset<<<1, 128, 0, s>>>(c->meta, c->cfg.batch, row);
-  return cudaGetLastError();
+  return kvc_launch_pdl(k_reset, dim3(1), dim3(128), 0, s, c->meta, c->cfg.batch, row);
 }
 
 cudaError_t kvc_launch_set_lengths(kvc_cache* c, const int32_t* kv_len, const int32_t* cu, cudaStream_t s) {
-  k_set_lengths<<<1, 128, 0, s>>>(c->meta, c->cfg.batch, c->cap, kv_len, cu);
-  return cudaGetLastError();
+  return kvc_launch_pdl(k_set_lengths, dim3(1), dim3(128), 0, s, c->meta, c->cfg.batch, c->cap, kv_len, cu);
 }
 
 cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
@@ -316,9 +322,8 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
   const int64_t max_blocks = (int64_t)c->num_sms * 8;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
-  k_write<<<(unsigned)blocks, kWriteThreads, 0, s>>>((const uint4*)k, (const uint4*)v, (uint4*)c->k, (uint4*)c->v,
-                                                     c->meta, slots, g.batch, n, row_vecs, c->cap, g.layout);
-  return cudaGetLastError();
+  return kvc_launch_pdl(k_write, dim3((unsigned)blocks), dim3(kWriteThreads), 0, s, (const uint4*)k, (const uint4*)v,
+                        (uint4*)c->k, (uint4*)c->v, c->meta, slots, g.batch, n, row_vecs, c->cap, g.layout);
 }
 
 cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,

@@ -157,6 +157,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   const int sub = lane & 7;          // dim slice
   const int grp = lane >> 3;         // row within the group of 4
 
+  kvc_pdl_wait();
+  kvc_pdl_release();
   int row0 = 0, len = 0;
   if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;
 
@@ -428,9 +430,8 @@ cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, cudaSt
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
-  k_decode<T, D, G><<<grid, kThreads, smem, s>>>(c->tm_dk, c->tm_dv, (const T*)q, (T*)out, c->meta, (float*)c->ws, g,
-                                                 c->scale * 1.4426950408889634f, lse);
-  return cudaGetLastError();
+  return kvc_launch_pdl(k_decode<T, D, G>, grid, dim3(kThreads), smem, s, c->tm_dk, c->tm_dv, (const T*)q, (T*)out,
+                        c->meta, (float*)c->ws, g, c->scale * 1.4426950408889634f, lse);
 }
 
 template <typename T, int D>

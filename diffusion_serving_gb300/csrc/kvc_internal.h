@@ -75,6 +75,31 @@ __device__ __forceinline__ int64_t kvc_kv_offset(const kvc_geom& g, int b, int r
   return (row * g.Hkv + kvh) * (int64_t)g.D;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Kernels launched through kvc_launch_pdl may start (be scheduled, run their first
+// instructions) while the previous kernel on the stream is still finishing; each of
+// them calls kvc_pdl_wait() before it touches any global memory, which blocks until
+// every prerequisite grid has completed and its writes are visible, so the stream
+// order of the data is unchanged.  kvc_pdl_release() lets the next such kernel start.
+__device__ __forceinline__ void kvc_pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void kvc_pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t kvc_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                           Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Most splits the decode kernel takes per (row, kv head).
 #define KVC_DECODE_MAX_SPLITS 1024
 
