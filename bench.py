@@ -284,6 +284,40 @@ def tc_traffic_per_launch(w, per_attend_kv):
     return round(cap["dram_over_algorithmic"] * (qo + float(np.mean(kv))))
 
 
+def cross_bench(kvc, peaks, reps=10):
+    """Ragged cross-attention (2 CFG branches, H 40, D 128, 75600 padded queries, packed
+    text K/V by cu_seqlens): time per attend for the three length skews.  Q and O
+    traffic (3.1 GB) bounds it; the roofline time is max(bytes / HBM, flops / tensor)."""
+    w = wl.CROSS
+    B, H, D, Lq = w.batch, w.heads, w.head_dim, wl.CROSS_LQ
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    q = torch.randn(B, Lq, H, D, device="cuda", generator=g).bfloat16()
+    out = torch.empty_like(q)
+    kv = torch.randn(B, wl.CROSS_LKV_MAX, H, D, device="cuda", generator=g).bfloat16()
+    res = {}
+    for name, lens in wl.CROSS_SKEWS.items():
+        c = kvc.KVCache(B, H, H, D, torch.bfloat16, "packed", capacity=2 * wl.CROSS_LKV_MAX)
+        c.set_lengths(cu_seqlens=torch.tensor(wl.seqlens_to_cu(lens), dtype=torch.int32, device="cuda"))
+        c.write(kv, kv)
+        for _ in range(3):
+            c.attend(q, out)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            c.attend(q, out)
+        b.record()
+        b.synchronize()
+        t = a.elapsed_time(b) * 1e-3 / reps
+        nbytes = 2 * q.numel() * 2 + sum(2 * n * H * D * 2 for n in lens)
+        flops = sum(wl.attention_flops(Lq, n, H, D) for n in lens)
+        roof = max(nbytes / (peaks["hbm"] * 1e9), flops / (peaks["bf16"] * 1e12))
+        res[name] = {"lens": list(lens), "ms": round(t * 1e3, 4), "GB/s": round(nbytes / t / 1e9, 1),
+                     "TFLOP/s": round(flops / t / 1e12, 1), "roofline_ms": round(roof * 1e3, 4),
+                     "frac": round(roof / t, 4)}
+        assert c.get_error() == 0
+    return res
+
+
 def cpu_oracle_sample(w, budget_s=12.0):
     """Time the fp64 oracle on sampled query rows of a full-window attend."""
     from oracle import kvc_oracle as orc
@@ -416,6 +450,7 @@ def ours(args):
     if clocks is not None:
         result["clocks"] = clocks
     result["decode"] = decode_bench(kvc, peaks)
+    result["cross_attention"] = cross_bench(kvc, peaks)
 
     # end to end through the binding: host (pinned) inputs copied in, output read back
     if True:

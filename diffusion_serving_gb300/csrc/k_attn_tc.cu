@@ -10,8 +10,8 @@
 // "pass only active KV cache prefix to SDPA", "Change"); with KVC_CAUSAL the query
 // at absolute position kv_len - n_q + i sees slots <= that position (same section).
 //
-// One CTA = two 128-row query tiles (A and B) of one (batch row, q head), sharing every
-// K/V tile it loads.  Warp roles (384 threads):
+// Work item = two 128-row query tiles (A and B) of one (batch row, q head), sharing every
+// K/V tile it loads.  The kernel is persistent: one CTA per SM walks the items.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles of 128 slots into a
 //               two-stage ring (128B-swizzled boxes of 64 dims x 128 slots).
 //   warp 1      TMEM owner and MMA issuer: S = Q K^T (A, B from shared memory) and
@@ -52,7 +52,7 @@ struct Smem {
   uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
-  uint64_t q_full;
+  uint64_t q_full, q_free;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[2], p_ready[2], o_done[2];
@@ -285,7 +285,39 @@ struct TcParams {
   float* lse;        // optional [B, n_q, H] natural-log log-sum-exp of each row's scaled scores
 };
 
+// Work item = one pair of 128-row query tiles (A, B) of one (batch row, q head), in the
+// order pair-fastest, then head, then row.  The same geometry is derived independently
+// by every role from the item index and the meta block.
+struct Item {
+  int b, h, kvh, row_a, row0, kv_batch, qpos0, kv_end, n_tiles;
+};
+
+__device__ __forceinline__ bool item_geom(int item, int pairs, const TcParams& p, int32_t* meta, Item* it) {
+  const kvc_geom& g = p.g;
+  const int pair = item % pairs, bh = item / pairs;
+  it->h = bh % g.H;
+  it->b = bh / g.H;
+  it->kvh = it->h / (g.H / g.Hkv);
+  it->row_a = pair * 2 * kBM;
+  int len = 0;
+  if (!kvc_row_range(meta, g, it->b, &it->row0, &len, meta + KVC_META_ERR)) return false;
+  it->kv_batch = g.layout == KVC_PACKED ? 0 : it->b;
+  it->qpos0 = len - p.n_q;                             // absolute position of query 0 (causal)
+  it->kv_end = len;
+  if (p.causal) {
+    const int last_row = min(it->row_a + 2 * kBM, p.n_q) - 1;
+    it->kv_end = max(1, min(len, it->qpos0 + last_row + 1));
+  }
+  it->n_tiles = (it->kv_end + kBN - 1) / kBN;
+  return true;
+}
+
 // ---- the kernel --------------------------------------------------------------
+// Persistent: one CTA per SM walks the work items item = blockIdx.x, + gridDim.x, ...
+// Barrier phases continue across items: K/V stages, S-ready and P-ready barriers count
+// K/V tiles over the CTA's whole run, the Q and O barriers count items.  The next
+// item's Q tiles load as soon as the current item's last QK MMA has completed, and its
+// first MMAs run while the softmax warps finish the current item's epilogue.
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -293,10 +325,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int row_a = blockIdx.x * 2 * kBM;
   const kvc_geom& g = p.g;
-  const int kvh = h / (g.H / g.Hkv);
+  const int pairs = (p.n_q + 2 * kBM - 1) / (2 * kBM);
+  const int n_items = g.B * g.H * pairs;
 
   // a CTA that starts after another one gave up on a wait returns at once (one read,
   // shared, so that every thread takes the same branch)
@@ -304,19 +335,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     sm.abort = (*reinterpret_cast<volatile int32_t*>(meta + KVC_META_ERR) & KVC_DEV_TIMEOUT) ? 1 : 0;
   __syncthreads();
   if (sm.abort) return;
-  int row0 = 0, len = 0;
-  if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;  // same outcome in every thread
-  const int qpos0 = len - p.n_q;                       // absolute position of query 0 (causal)
-  int kv_end = len;
-  if (p.causal) {
-    const int last_row = min(row_a + 2 * kBM, p.n_q) - 1;
-    kv_end = max(1, min(len, qpos0 + last_row + 1));
-  }
-  const int n_tiles = (kv_end + kBN - 1) / kBN;
   volatile int* abort = &sm.abort;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_free, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
@@ -339,32 +362,49 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  const int kv_batch = g.layout == KVC_PACKED ? 0 : b;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      mbar_expect_tx(&sm.q_full, 2 * kTileBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(&tm_q, &sm.q_full, sm.q[t] + half * kBoxBytes, half * 64, h, row_a + t * kBM, b);
-      int k_issued = 0, v_issued = 0;
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kStages, u = j / kStages;
-        if (j >= kStages && !mbar_wait(&sm.k_empty[s], (u - 1) & 1, abort)) break;
-        mbar_expect_tx(&sm.k_full[s], kTileBytes);
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(&tm_k, &sm.k_full[s], sm.k[s] + half * kBoxBytes, half * 64, kvh, row0 + j * kBN, kv_batch);
-        k_issued = j + 1;
-        if (j >= kStages && !mbar_wait(&sm.v_empty[s], (u - 1) & 1, abort)) break;
-        mbar_expect_tx(&sm.v_full[s], kTileBytes);
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(&tm_v, &sm.v_full[s], sm.v[s] + half * kBoxBytes, half * 64, kvh, row0 + j * kBN, kv_batch);
-        v_issued = j + 1;
+      int T = 0, n_items_done = 0;           // K/V tiles and items issued so far
+      int k_issued = 0, v_issued = 0, q_issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        Item I;
+        if (!item_geom(item, pairs, p, meta, &I)) continue;
+        // the previous item's Q tiles are free once its last QK MMA completed
+        if (n_items_done > 0 && !mbar_wait(&sm.q_free, (n_items_done - 1) & 1, abort)) break;
+        mbar_expect_tx(&sm.q_full, 2 * kTileBytes);
+        for (int t = 0; t < 2; ++t)
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(&tm_q, &sm.q_full, sm.q[t] + half * kBoxBytes, half * 64, I.h, I.row_a + t * kBM, I.b);
+        q_issued = n_items_done + 1;
+        for (int j = 0; j < I.n_tiles; ++j) {
+          const int Tj = T + j, s = Tj % kStages, u = Tj / kStages;
+          const int row = I.row0 + j * kBN;
+          if (Tj >= kStages && !mbar_wait(&sm.k_empty[s], (u - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.k_full[s], kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(&tm_k, &sm.k_full[s], sm.k[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
+          k_issued = Tj + 1;
+          if (Tj >= kStages && !mbar_wait(&sm.v_empty[s], (u - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.v_full[s], kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(&tm_v, &sm.v_full[s], sm.v[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
+          v_issued = Tj + 1;
+        }
+        T += I.n_tiles;
+        ++n_items_done;
       }
       if (*abort) {
         // drain: every load this thread issued lands before the CTA's shared memory is released
-        mbar_wait(&sm.q_full, 0, abort, false);
+        if (q_issued > 0) mbar_wait(&sm.q_full, (q_issued - 1) & 1, abort, false);
         for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
           mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, abort, false);
         for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
@@ -391,66 +431,76 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
                (j > 0 || kk > 0) ? 1u : 0u);
     };
-    bool ok = mbar_wait(&sm.q_full, 0, abort) && mbar_wait(&sm.k_full[0], 0, abort);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
+    int T = 0, n_items_done = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      Item I;
+      if (!item_geom(item, pairs, p, meta, &I)) continue;
+      const int s0 = T % kStages, u0 = T / kStages;
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, n_items_done & 1, abort) &&
+                                       mbar_wait(&sm.k_full[s0], u0 & 1, abort));
+      if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        issue_qk(0, 0);
+        issue_qk(0, s0);
         mma_commit(&sm.s_full[0]);
-        issue_qk(1, 0);
+        issue_qk(1, s0);
         mma_commit(&sm.s_full[1]);
-        mma_commit(&sm.k_empty[0]);
+        mma_commit(&sm.k_empty[s0]);
+        if (I.n_tiles == 1) mma_commit(&sm.q_free);
       }
       __syncwarp();
-    }
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kStages, u = j / kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
-      if (!ok) break;
-      const int rem = kv_end - j * kBN;
-      if (rem < kBN) {
-        // slots past the valid range may hold anything (NaN included): zero those V rows
-        // so that P = 0 there contributes exactly nothing
-        for (int e = lane; e < (kBN - rem) * 2 * 8; e += 32) {
-          const int r = rem + e / 16, half = (e / 8) & 1, c = e & 7;
-          *reinterpret_cast<uint4*>(sm.v[s] + half * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+      for (int j = 0; ok && j < I.n_tiles; ++j) {
+        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
+        if (!ok) break;
+        const int rem = I.kv_end - j * kBN;
+        if (rem < kBN) {
+          // slots past the valid range may hold anything (NaN included): zero those V rows
+          // so that P = 0 there contributes exactly nothing
+          for (int e = lane; e < (kBN - rem) * 2 * 8; e += 32) {
+            const int r = rem + e / 16, half = (e / 8) & 1, c = e & 7;
+            *reinterpret_cast<uint4*>(sm.v[s] + half * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+          __syncwarp();
         }
-        fence_proxy_async();
-        __syncwarp();
-      }
-      const bool more = j + 1 < n_tiles;
-      const int s1 = (j + 1) % kStages, u1 = (j + 1) / kStages;
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[0], j & 1, abort));
-      if (!ok) break;
-      tc_fence_after();
-      if (lane == 0) issue_pv(0, s, j);
-      if (more) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s1], u1 & 1, abort));
+        const bool more = j + 1 < I.n_tiles;
+        const int s1 = (Tj + 1) % kStages, u1 = (Tj + 1) / kStages;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[0], Tj & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) issue_pv(0, s, j);
+        if (more) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s1], u1 & 1, abort));
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) {
+            issue_qk(0, s1);
+            mma_commit(&sm.s_full[0]);
+          }
+        } else if (lane == 0) {
+          mma_commit(&sm.o_done[0]);
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[1], Tj & 1, abort));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          issue_qk(0, s1);
-          mma_commit(&sm.s_full[0]);
+          issue_pv(1, s, j);
+          mma_commit(&sm.v_empty[s]);
+          if (more) {
+            issue_qk(1, s1);
+            mma_commit(&sm.s_full[1]);
+            mma_commit(&sm.k_empty[s1]);
+            if (j + 2 == I.n_tiles) mma_commit(&sm.q_free);   // that was this item's last QK
+          } else {
+            mma_commit(&sm.o_done[1]);
+          }
         }
-      } else if (lane == 0) {
-        mma_commit(&sm.o_done[0]);
+        __syncwarp();
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[1], j & 1, abort));
-      if (!ok) break;
-      tc_fence_after();
-      if (lane == 0) {
-        issue_pv(1, s, j);
-        mma_commit(&sm.v_empty[s]);
-        if (more) {
-          issue_qk(1, s1);
-          mma_commit(&sm.s_full[1]);
-          mma_commit(&sm.k_empty[s1]);
-        } else {
-          mma_commit(&sm.o_done[1]);
-        }
-      }
-      __syncwarp();
+      T += I.n_tiles;
+      ++n_items_done;
     }
     if (*abort && lane == 0) {
       // drain: all MMAs issued by this thread complete before TMEM is released
@@ -463,68 +513,74 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const int t = (warp - 4) >> 2;          // query tile A or B
     const int quad = warp & 3;              // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;         // row within the tile
-    const int row = row_a + t * kBM + r;    // query row within the chunk
     const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
     const uint32_t s_addr = lane_addr + (t ? 128u : 0u);
     const uint32_t o_addr = lane_addr + (t ? 384u : 256u);
     const float c = p.scale_log2;
-    const int qpos = qpos0 + row;
-    float m_ref = -INFINITY, l = 0.f;
+    int T = 0, n_items_done = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, abort));
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[128];
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      Item I;
+      if (!item_geom(item, pairs, p, meta, &I)) continue;
+      const int row = I.row_a + t * kBM + r;   // query row within the chunk
+      const int qpos = I.qpos0 + row;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < I.n_tiles; ++j) {
+        const int Tj = T + j;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], Tj & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[128];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_addr + q4 * 32, sr + q4 * 32);
-      tmem_ld_wait();
+        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_addr + q4 * 32, sr + q4 * 32);
+        tmem_ld_wait();
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr + q4 * 32);
-      int valid = kv_end - j * kBN;                          // columns < valid are slots in range
-      if (p.causal) valid = min(valid, qpos - j * kBN + 1);
-      const bool full = !p.causal && kv_end - j * kBN >= kBN;    // uniform: no column masked
-      const float mx = full ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
-      const float m_tile = mx * c;
-      bool rescale = m_tile > m_ref + kRescaleThreshold;
-      const float m_new = rescale ? m_tile : m_ref;
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      if (__any_sync(0xffffffffu, rescale) && j > 0) {
-        const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
+        for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr + q4 * 32);
+        int valid = I.kv_end - j * kBN;                          // columns < valid are slots in range
+        if (p.causal) valid = min(valid, qpos - j * kBN + 1);
+        const bool full = !p.causal && I.kv_end - j * kBN >= kBN;   // uniform: no column masked
+        const float mx = full ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
+        const float m_tile = mx * c;
+        bool rescale = m_tile > m_ref + kRescaleThreshold;
+        const float m_new = rescale ? m_tile : m_ref;
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        if (__any_sync(0xffffffffu, rescale) && j > 0) {
+          const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
 #pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t orow[32];
-          tmem_ld32(o_addr + q4 * 32, orow);
-          tmem_ld_wait();
-          reg_fence32(orow);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t orow[32];
+            tmem_ld32(o_addr + q4 * 32, orow);
+            tmem_ld_wait();
+            reg_fence32(orow);
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[i]), __uint_as_float(orow[i + 1])),
-                                        make_float2(alpha, alpha));
-            orow[i] = __float_as_uint(y.x);
-            orow[i + 1] = __float_as_uint(y.y);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[i]), __uint_as_float(orow[i + 1])),
+                                          make_float2(alpha, alpha));
+              orow[i] = __float_as_uint(y.x);
+              orow[i + 1] = __float_as_uint(y.y);
+            }
+            tmem_st32(o_addr + q4 * 32, orow);
           }
-          tmem_st32(o_addr + q4 * 32, orow);
+          tmem_st_wait();
+          l *= alpha;
         }
+        m_ref = m_new;
+        l += full ? exp_pack_store<kBf16, false>(sr, valid, c, m_use, s_addr)
+                  : exp_pack_store<kBf16, true>(sr, valid, c, m_use, s_addr);
         tmem_st_wait();
-        l *= alpha;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_ready[t]);
       }
-      m_ref = m_new;
-      l += full ? exp_pack_store<kBf16, false>(sr, valid, c, m_use, s_addr)
-                : exp_pack_store<kBf16, true>(sr, valid, c, m_use, s_addr);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.p_ready[t]);
-    }
-    ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], 0, abort));
-    if (ok) {
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], n_items_done & 1, abort));
+      if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const bool store = row < p.n_q;
       if (p.lse != nullptr && store)   // m_ref and l are in the exp2 domain of scale * q.k
-        p.lse[((int64_t)b * p.n_q + row) * g.H + h] = l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
-      uint16_t* dst = reinterpret_cast<uint16_t*>(out) + (((int64_t)b * p.n_q + row) * g.H + h) * kD;
+        p.lse[((int64_t)I.b * p.n_q + row) * g.H + I.h] =
+            l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(out) + (((int64_t)I.b * p.n_q + row) * g.H + I.h) * kD;
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t orow[32];
@@ -544,6 +600,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         }
       }
+      // O of this item has been read: the issuer may overwrite it once this warp's next
+      // P-ready arrives (program order), so no separate signal is needed
+      tc_fence_before();
+      T += I.n_tiles;
+      ++n_items_done;
     }
   }
 
@@ -594,7 +655,9 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
   p.causal = causal ? 1 : 0;
   p.scale_log2 = c->scale * 1.4426950408889634f;
   p.lse = lse;
-  dim3 grid((n_q + 2 * kBM - 1) / (2 * kBM), cfg.heads, cfg.batch);
+  const int64_t items = (int64_t)((n_q + 2 * kBM - 1) / (2 * kBM)) * cfg.heads * cfg.batch;
+  if (items > INT32_MAX) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)(items < c->num_sms ? items : c->num_sms));    // persistent: one CTA per SM
   if (cfg.dtype == KVC_BF16)
     k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, out, c->meta, p);
   else
