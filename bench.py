@@ -284,12 +284,12 @@ def tc_traffic_per_launch(w, per_attend_kv):
     return round(cap["dram_over_algorithmic"] * (qo + float(np.mean(kv))))
 
 
-def cross_bench(kvc, peaks, reps=10):
+def cross_bench(kvc, peaks, reps=10, lq=None):
     """Ragged cross-attention (2 CFG branches, H 40, D 128, 75600 padded queries, packed
     text K/V by cu_seqlens): time per attend for the three length skews.  Q and O
     traffic (3.1 GB) bounds it; the roofline time is max(bytes / HBM, flops / tensor)."""
     w = wl.CROSS
-    B, H, D, Lq = w.batch, w.heads, w.head_dim, wl.CROSS_LQ
+    B, H, D, Lq = w.batch, w.heads, w.head_dim, lq or wl.CROSS_LQ
     g = torch.Generator(device="cuda").manual_seed(w.seed)
     q = torch.randn(B, Lq, H, D, device="cuda", generator=g).bfloat16()
     out = torch.empty_like(q)
@@ -541,7 +541,15 @@ def main():
                     help="seconds of CPU oracle work per step of the reference arm (a bounded sample)")
     ap.add_argument("--pool", type=int, default=8,
                     help="distinct (q, k, v) input sets, reused cyclically over the chunks")
+    ap.add_argument("--cross-only", action="store_true",
+                    help="time only the ragged cross-attention attends and print them (profiling aid)")
+    ap.add_argument("--cross-lq", type=int, default=None,
+                    help="padded query count of the cross-attention timing (default: the full workload)")
     args = ap.parse_args()
+    if args.cross_only:
+        from diffusion_serving_gb300 import kvc
+        print(json.dumps({"cross_attention": cross_bench(kvc, load_peaks(), reps=args.steps, lq=args.cross_lq)}))
+        return
     if args.impl == "reference":
         reference(args)
     else:

@@ -44,6 +44,7 @@ constexpr int kStages = 2;
 constexpr int kThreads = 384;
 constexpr uint32_t kBoxBytes = 64 * 2 * 128;         // 64 dims x 128 rows, 16-bit
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;       // 128 dims
+constexpr uint32_t kStageBytes = 32 * 32 * 2;        // 32 rows x 32 dims, 16-bit
 constexpr uint64_t kTimeoutNs = 500000000ull;   // 0.5 s; a healthy wait is microseconds
 constexpr float kRescaleThreshold = 8.0f;            // log2 units
 
@@ -52,6 +53,9 @@ struct Smem {
   uint8_t q[2][kTileBytes];
   uint8_t k[kStages][kTileBytes];
   uint8_t v[kStages][kTileBytes];
+  // output staging: per softmax warp two 32-row x 32-column buffers (64-byte swizzle),
+  // written to global memory by TMA stores
+  uint8_t o_stage[8][2][kStageBytes];
   uint64_t q_full, q_free;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
@@ -60,6 +64,9 @@ struct Smem {
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory above the 227 KB a block may opt into");
+static_assert(offsetof(Smem, o_stage) % 1024 == 0, "staging buffers must keep the swizzle phase of their address");
 
 // ---- PTX wrappers ----------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -120,6 +127,19 @@ __device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* ba
       "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Bulk tensor store of one box from shared memory; completion tracked by bulk groups.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%1, %2, %3, %4}], [%5];" ::"l"(map),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most one committed bulk group still reads its shared-memory source
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// wait until every committed bulk group has completed its writes
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -292,15 +312,28 @@ struct Item {
   int b, h, kvh, row_a, row0, kv_batch, qpos0, kv_end, n_tiles;
 };
 
-__device__ __forceinline__ bool item_geom(int item, int pairs, const TcParams& p, int32_t* meta, Item* it) {
+// Row range of the last batch row looked up (consecutive items of a CTA mostly share
+// it), so that the meta block is read once per row and role rather than once per item.
+struct RowCache {
+  int b = -1, row0 = 0, len = 0;
+  bool ok = false;
+};
+
+__device__ __forceinline__ bool item_geom(int item, int pairs, const TcParams& p, int32_t* meta, RowCache& rc,
+                                          Item* it) {
   const kvc_geom& g = p.g;
   const int pair = item % pairs, bh = item / pairs;
   it->h = bh % g.H;
   it->b = bh / g.H;
   it->kvh = it->h / (g.H / g.Hkv);
   it->row_a = pair * 2 * kBM;
-  int len = 0;
-  if (!kvc_row_range(meta, g, it->b, &it->row0, &len, meta + KVC_META_ERR)) return false;
+  if (it->b != rc.b) {
+    rc.b = it->b;
+    rc.ok = kvc_row_range(meta, g, it->b, &rc.row0, &rc.len, meta + KVC_META_ERR);
+  }
+  if (!rc.ok) return false;
+  const int len = rc.len;
+  it->row0 = rc.row0;
   it->kv_batch = g.layout == KVC_PACKED ? 0 : it->b;
   it->qpos0 = len - p.n_q;                             // absolute position of query 0 (causal)
   it->kv_end = len;
@@ -321,7 +354,8 @@ __device__ __forceinline__ bool item_geom(int item, int pairs, const TcParams& p
 template <bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-          const __grid_constant__ CUtensorMap tm_v, void* __restrict__ out, int32_t* __restrict__ meta, TcParams p) {
+          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+          int32_t* __restrict__ meta, TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -367,11 +401,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       int T = 0, n_items_done = 0;           // K/V tiles and items issued so far
+      RowCache rc;
       int k_issued = 0, v_issued = 0, q_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         Item I;
-        if (!item_geom(item, pairs, p, meta, &I)) continue;
+        if (!item_geom(item, pairs, p, meta, rc, &I)) continue;
         // the previous item's Q tiles are free once its last QK MMA completed
         if (n_items_done > 0 && !mbar_wait(&sm.q_free, (n_items_done - 1) & 1, abort)) break;
         mbar_expect_tx(&sm.q_full, 2 * kTileBytes);
@@ -432,10 +467,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                (j > 0 || kk > 0) ? 1u : 0u);
     };
     int T = 0, n_items_done = 0;
+    RowCache rc;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       Item I;
-      if (!item_geom(item, pairs, p, meta, &I)) continue;
+      if (!item_geom(item, pairs, p, meta, rc, &I)) continue;
       const int s0 = T % kStages, u0 = T / kStages;
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, n_items_done & 1, abort) &&
                                        mbar_wait(&sm.k_full[s0], u0 & 1, abort));
@@ -517,11 +553,13 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     const uint32_t s_addr = lane_addr + (t ? 128u : 0u);
     const uint32_t o_addr = lane_addr + (t ? 384u : 256u);
     const float c = p.scale_log2;
+    uint8_t* const stage = sm.o_stage[warp - 4][0];
     int T = 0, n_items_done = 0;
+    RowCache rc;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       Item I;
-      if (!item_geom(item, pairs, p, meta, &I)) continue;
+      if (!item_geom(item, pairs, p, meta, rc, &I)) continue;
       const int row = I.row_a + t * kBM + r;   // query row within the chunk
       const int qpos = I.qpos0 + row;
       float m_ref = -INFINITY, l = 0.f;
@@ -576,11 +614,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      const bool store = row < p.n_q;
-      if (p.lse != nullptr && store)   // m_ref and l are in the exp2 domain of scale * q.k
+      if (p.lse != nullptr && row < p.n_q)   // m_ref and l are in the exp2 domain of scale * q.k
         p.lse[((int64_t)I.b * p.n_q + row) * g.H + I.h] =
             l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
-      uint16_t* dst = reinterpret_cast<uint16_t*>(out) + (((int64_t)I.b * p.n_q + row) * g.H + I.h) * kD;
+      // O rows -> 64-byte-swizzled staging (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3),
+      // conflict-free) -> one TMA store per 32 columns; rows past n_q are clipped by the map
+      const int grow = I.row_a + t * kBM + quad * 32;    // first query row of this warp
 #pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t orow[32];
@@ -594,10 +633,18 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
                                       make_float2(inv, inv));
           pk[i] = pack2<kBf16>(y.x, y.y);
         }
-        if (store) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + q4 * 32);
+        uint8_t* buf = stage + (q4 & 1) * kStageBytes;
+        if (lane == 0) bulk_wait_read1();                // the store that last read buf is done with it
+        __syncwarp();
 #pragma unroll
-          for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
+              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&tm_o, buf, q4 * 32, I.h, grow, I.b);
+          bulk_commit();
         }
       }
       // O of this item has been read: the issuer may overwrite it once this warp's next
@@ -606,6 +653,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       T += I.n_tiles;
       ++n_items_done;
     }
+    if (lane == 0) bulk_wait_all();                      // staging stays live until the stores land
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -648,7 +697,10 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
                                cudaStream_t s) {
   const kvc_config& cfg = c->cfg;
   CUtensorMap tm_q;
+  CUtensorMap tm_o;
   if (!make_map(&tm_q, cfg.dtype, q, cfg.heads, (uint64_t)n_q, cfg.batch)) return cudaErrorInvalidValue;
+  if (!kvc_make_tile_map(&tm_o, cfg.dtype, out, kD, cfg.heads, (uint64_t)n_q, cfg.batch, 32, KVC_BOX_SW64))
+    return cudaErrorInvalidValue;
   TcParams p;
   p.g = kvc_geom{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
   p.n_q = n_q;
@@ -659,8 +711,8 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   dim3 grid((unsigned)(items < c->num_sms ? items : c->num_sms));    // persistent: one CTA per SM
   if (cfg.dtype == KVC_BF16)
-    k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, out, c->meta, p);
+    k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
   else
-    k_attn_tc<false><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, out, c->meta, p);
+    k_attn_tc<false><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
   return cudaGetLastError();
 }

@@ -490,8 +490,9 @@ cudaError_t kvc_prepare_decode(kvc_cache* c) { return prepare_once(c); }
 bool kvc_make_decode_maps(kvc_cache* c) {
   const kvc_config& g = c->cfg;
   const uint64_t batches = g.layout == KVC_PACKED ? 1 : (uint64_t)g.batch;
-  return kvc_make_tile_map(&c->tm_dk, g.dtype, c->k, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile, true) &&
-         kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, (uint64_t)c->cap, batches, kTile, true);
+  const uint64_t cap = (uint64_t)c->cap;
+  return kvc_make_tile_map(&c->tm_dk, g.dtype, c->k, g.head_dim, g.kv_heads, cap, batches, kTile, KVC_BOX_ROWS) &&
+         kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, cap, batches, kTile, KVC_BOX_ROWS);
 }
 
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s) {
