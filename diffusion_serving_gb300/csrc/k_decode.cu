@@ -39,7 +39,7 @@ constexpr int kRowsPerWarp = kGroups * 4;   // 16 rows of every tile per consume
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
 constexpr int kMinShare = 64;               // fewest slots a block takes (short prefixes use few splits)
 constexpr int kTile = kWarps * kRowsPerWarp;  // 112 slots per stage (one TMA box of rows: 14 swizzle atoms)
-constexpr int kStages = 3;                  // 3 x 56 KB in flight per SM (bandwidth x latency)
+constexpr int kStages = 4;                  // 4 x 56 KB in flight per SM (bandwidth x loaded latency)
 constexpr uint64_t kTimeoutNs = 500000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -100,23 +100,44 @@ __device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* ba
       : "memory");
 }
 
-__device__ __forceinline__ void unpack8(const uint4& u, float* f, const __half*) {
-  const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 x = __half22float2(h[i]);
-    f[2 * i] = x.x;
-    f[2 * i + 1] = x.y;
-  }
+// ---- warp-level MMA (m16n8k16, 16-bit inputs, fp32 accumulate) -----------------
+// ldmatrix reads shared memory that TMA filled: volatile keeps it after the barrier wait.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-__device__ __forceinline__ void unpack8(const uint4& u, float* f, const __nv_bfloat16*) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float2 x = __bfloat1622float2(h[i]);
-    f[2 * i] = x.x;
-    f[2 * i + 1] = x.y;
-  }
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+// d += A B for A = 16 x 16 (row-major fragment a0..a3, here rows 8..15 are zero: the
+// padding of the head dimension) and B = 16 x 8 (fragment b0, b1).
+template <typename T>
+__device__ __forceinline__ void mma16816(float* d, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<__half>(float* d, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<__nv_bfloat16>(float* d, uint32_t a0, uint32_t a2, uint32_t b0,
+                                                        uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, const __half*) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, const __nv_bfloat16*) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 __device__ __forceinline__ void store_out(__half* p, float x) { *p = __float2half_rn(x); }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
@@ -127,10 +148,12 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// K and V tiles are staged as 128-byte-swizzled boxes of 64 dims x kTile slots: 16-byte
+// chunk c of slot r sits at chunk c ^ (r & 7) of the slot's 128-byte line, so the 8 row
+// addresses of every ldmatrix hit 8 different bank groups.
+constexpr uint32_t kHalfBytes = kTile * 128u;                                            // one 64-dim box
 template <int D>
-__host__ __device__ constexpr uint32_t box_bytes() { return kTile * D * 2u; }         // kTile whole rows
-template <int D>
-__host__ __device__ constexpr uint32_t stage_bytes() { return 2u * box_bytes<D>(); }  // K and V
+__host__ __device__ constexpr uint32_t stage_bytes() { return 2u * (D / 64) * kHalfBytes; }  // K and V
 template <int D>
 __host__ __device__ constexpr size_t dyn_smem_bytes() { return (size_t)kStages * stage_bytes<D>() + 1024; }
 
@@ -139,14 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const T* __restrict__ q,
          T* __restrict__ out, int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2,
          float* __restrict__ lse) {
-  constexpr int VPL = D / 64;        // 16-byte vectors (= 64-dim boxes) per lane per row
-  constexpr int EPL = VPL * 8;       // dims per lane
-  constexpr uint32_t BOX = box_bytes<D>();
+  constexpr int HB = D / 64;         // 64-dim boxes per K (or V) tile
+  constexpr int NT = D / 8;          // n-tiles of 8 dims in O
   constexpr uint32_t SB = stage_bytes<D>();
   extern __shared__ uint8_t dsm_raw[];
   uint8_t* dsm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) & ~(uintptr_t)1023);
   __shared__ uint64_t full[kStages], empty[kStages];
-  __shared__ float s_acc[kWarps][G][D];
+  // per-warp partial accumulators [kWarps][G][D]: the stage ring, once every warp is past it
+  float (*s_acc)[G][D] = reinterpret_cast<float (*)[G][D]>(dsm);
   __shared__ float s_ml[kWarps][G][2];
   __shared__ float s_inv[G];
   __shared__ int s_last, s_abort;
@@ -154,8 +177,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   const int split = blockIdx.x, nsplit = gridDim.x;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int sub = lane & 7;          // dim slice
-  const int grp = lane >> 3;         // row within the group of 4
+  const int hq = lane >> 2;          // head row of this lane in the MMA fragments (real if < G)
+  const int quad = lane & 3;         // column pair within the fragments
 
   kvc_pdl_wait();
   kvc_pdl_release();
@@ -189,8 +212,11 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         mbar_expect_tx(&full[st], SB);
         uint8_t* dst = dsm + st * SB;
         const int row = row0 + t0 + t * kTile;
-        tma_load_4d(&tm_k, &full[st], dst, 0, kvh, row, kv_batch);
-        tma_load_4d(&tm_v, &full[st], dst + BOX, 0, kvh, row, kv_batch);
+#pragma unroll
+        for (int h = 0; h < HB; ++h) {
+          tma_load_4d(&tm_k, &full[st], dst + h * kHalfBytes, 64 * h, kvh, row, kv_batch);
+          tma_load_4d(&tm_v, &full[st], dst + (HB + h) * kHalfBytes, 64 * h, kvh, row, kv_batch);
+        }
         issued = t + 1;
       }
       if (*abort) {   // let every load issued here land before the block releases its shared memory
@@ -200,143 +226,118 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     }
   }
 
-  // query slice for this lane's dims, G heads, pre-scaled into the exp2 domain
-  float qv[G][EPL];
-  float m[G], l[G], acc[G][EPL];
+  // Per warp and tile: S = Q K^T on this warp's 16 slots (M = heads padded to 16, N = 8
+  // slots per MMA, K = 16 dims per MMA), online softmax per head row, O += P V (M = heads,
+  // N = 8 dims, K = the 16 slots).  The S fragment of two slot n-tiles is the P fragment
+  // of the PV MMA, so P never leaves registers.  Lane: head row hq, slots/dims 2 quad, +1.
+  uint32_t qa[D / 16][2];            // A fragments of Q (unscaled; rows 8..15 are zero)
+  float o[NT][4];                    // O fragments: rows hq (real heads) and hq + 8 (padding)
+  float m = -INFINITY, l = 0.f;      // running max (exp2 domain) and sum of this lane's head row
   if (warp < kWarps) {
+    const T* qp = q + ((int64_t)b * g.H + kvh * G + (hq < G ? hq : 0)) * D + 2 * quad;
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      const T* qp = q + ((int64_t)b * g.H + kvh * G + gg) * D;
-#pragma unroll
-      for (int v = 0; v < VPL; ++v) {
-        uint4 u = __ldg(reinterpret_cast<const uint4*>(qp + 64 * v + 8 * sub));
-        unpack8(u, &qv[gg][8 * v], (const T*)nullptr);
-      }
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) qv[gg][e] *= scale_log2;
-      m[gg] = -INFINITY;
-      l[gg] = 0.f;
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[gg][e] = 0.f;
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qa[kk][0] = hq < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk)) : 0u;
+      qa[kk][1] = hq < G ? __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 8)) : 0u;
     }
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
+    const int r0 = warp * 16;                              // this warp's slots of every tile
     for (int t = 0; t < n_tiles; ++t) {
       const int st = t % kStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (t / kStages) & 1, abort))) break;
-      const uint8_t* kst = dsm + st * SB;
-      const uint8_t* vst = kst + BOX;
-      const int first = t * kTile + warp * kRowsPerWarp;   // this warp's rows of the tile
+      const uint32_t kbase = smem_u32(dsm + st * SB);
+      const uint32_t vbase = kbase + HB * kHalfBytes;
+      const int first = t * kTile + r0;                    // split-relative index of slot r0
       if (first < nt) {
-        // scores of the warp's kGroups row groups (independent: they overlap in flight)
-        float sc[kGroups][G];
+        if (first + 16 > nt) {
+          // slots past the valid range may hold anything (NaN included): zero their V rows
+          // so that P = 0 there contributes exactly nothing
+          uint8_t* vrow = dsm + st * SB + HB * kHalfBytes;
+          for (int e = lane; e < 16 * HB * 8; e += 32) {
+            const int r = r0 + e / (HB * 8), h = (e / 8) % HB, c = e % 8;
+            if (t * kTile + r >= nt) *reinterpret_cast<uint4*>(vrow + h * kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA reuses the stage
+          __syncwarp();
+        }
+        // S: ldmatrix x4 = (slots r0..7 | r0+8..15) x (dims 16kk..+7 | +8..+15)
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          const int j = lane >> 3, i = lane & 7;
+          const int slot = r0 + (j >> 1) * 8 + i;
 #pragma unroll
-        for (int u = 0; u < kGroups; ++u) {
-          const int r = warp * kRowsPerWarp + u * 4 + grp;          // row within the tile
-          const uint32_t off = r * (D * 2) + sub * 16;                // 16-byte chunk `sub` of each 64-dim half
-          float kf[EPL];
-#pragma unroll
-          for (int v = 0; v < VPL; ++v)
-            unpack8(*reinterpret_cast<const uint4*>(kst + off + v * 128), &kf[8 * v], (const T*)nullptr);
-#pragma unroll
-          for (int gg = 0; gg < G; ++gg) {
-            float2 a2 = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int e = 0; e < EPL; e += 2)
-              a2 = __ffma2_rn(make_float2(qv[gg][e], qv[gg][e + 1]), make_float2(kf[e], kf[e + 1]), a2);
-            sc[u][gg] = a2.x + a2.y;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int chunk = (kk & 3) * 2 + (j & 1);
+            uint32_t bk[4];
+            ldsm_x4(kbase + (kk >> 2) * kHalfBytes + slot * 128 + ((chunk ^ (slot & 7)) << 4), bk);
+            mma16816<T>(sc[0], qa[kk][0], qa[kk][1], bk[0], bk[1]);
+            mma16816<T>(sc[1], qa[kk][0], qa[kk][1], bk[2], bk[3]);
           }
         }
+        // online softmax of head row hq over the warp's 16 slots
+        float x[4];
 #pragma unroll
-        for (int u = 0; u < kGroups; ++u)
+        for (int e = 0; e < 4; ++e) {
+          const int sl = first + (e >> 1) * 8 + 2 * quad + (e & 1);
+          x[e] = sl < nt ? sc[e >> 1][e & 1] * scale_log2 : -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        if (mx > m) {                                      // the running max grows
+          const float alpha = ex2(m - mx);                 // 0 on the first tile (m = -inf)
+          m = mx;
+          l *= alpha;
 #pragma unroll
-          for (int gg = 0; gg < G; ++gg) {
-            float a = sc[u][gg];
-            a += __shfl_xor_sync(0xffffffffu, a, 1);
-            a += __shfl_xor_sync(0xffffffffu, a, 2);
-            a += __shfl_xor_sync(0xffffffffu, a, 4);
-            sc[u][gg] = first + u * 4 + grp < nt ? a : -INFINITY;
-          }
-        // online softmax update per head, then P.V with V re-read from shared memory
-        float p[kGroups][G];
-#pragma unroll
-        for (int gg = 0; gg < G; ++gg) {
-          float mx = sc[0][gg];
-#pragma unroll
-          for (int u = 1; u < kGroups; ++u) mx = fmaxf(mx, sc[u][gg]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          if (mx > m[gg]) {                                // warp-uniform: the running max grows
-            const float alpha = ex2(m[gg] - mx);           // 0 on the first tile (m = -inf)
-            m[gg] = mx;
-            l[gg] *= alpha;
-#pragma unroll
-            for (int e = 0; e < EPL; e += 2) {
-              const float2 y = __fmul2_rn(make_float2(acc[gg][e], acc[gg][e + 1]), make_float2(alpha, alpha));
-              acc[gg][e] = y.x;
-              acc[gg][e + 1] = y.y;
-            }
-          }
-#pragma unroll
-          for (int u = 0; u < kGroups; ++u) {
-            p[u][gg] = ex2(sc[u][gg] - m[gg]);
-            l[gg] += p[u][gg];
+          for (int n = 0; n < NT; ++n) {
+            o[n][0] *= alpha;
+            o[n][1] *= alpha;
           }
         }
-        const bool partial = first + kRowsPerWarp > nt;     // stale rows past nt: their V is zeroed
+        float pr[4];
 #pragma unroll
-        for (int u = 0; u < kGroups; ++u) {
-          const int r = warp * kRowsPerWarp + u * 4 + grp;
-          const uint32_t off = r * (D * 2) + sub * 16;
-          float vf[EPL];
+        for (int e = 0; e < 4; ++e) {
+          pr[e] = ex2(x[e] - m);
+          l += pr[e];
+        }
+        const uint32_t pa0 = pack2(pr[0], pr[1], (const T*)nullptr);   // slots 2 quad, +1
+        const uint32_t pa2 = pack2(pr[2], pr[3], (const T*)nullptr);   // slots 8 + 2 quad, +1
+        // O += P V: ldmatrix.trans x4 = (slots r0..7 | r0+8..15) x (dims 8n..+7 | 8n+8..+15)
+        {
+          const int j = lane >> 3, i = lane & 7;
+          const int slot = r0 + (j & 1) * 8 + i;
 #pragma unroll
-          for (int v = 0; v < VPL; ++v)
-            unpack8(*reinterpret_cast<const uint4*>(vst + off + v * 128), &vf[8 * v], (const T*)nullptr);
-          if (partial && first + u * 4 + grp >= nt) {
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) vf[e] = 0.f;
+          for (int n = 0; n < NT; n += 2) {
+            const int chunk = (n & 7) + (j >> 1);
+            uint32_t bv[4];
+            ldsm_x4_t(vbase + (n >> 3) * kHalfBytes + slot * 128 + ((chunk ^ (slot & 7)) << 4), bv);
+            mma16816<T>(o[n], pa0, pa2, bv[0], bv[1]);
+            mma16816<T>(o[n + 1], pa0, pa2, bv[2], bv[3]);
           }
-#pragma unroll
-          for (int gg = 0; gg < G; ++gg)
-#pragma unroll
-            for (int e = 0; e < EPL; e += 2) {
-              const float2 y = __ffma2_rn(make_float2(p[u][gg], p[u][gg]), make_float2(vf[e], vf[e + 1]),
-                                          make_float2(acc[gg][e], acc[gg][e + 1]));
-              acc[gg][e] = y.x;
-              acc[gg][e + 1] = y.y;
-            }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);           // this warp is done with the stage
     }
-    // Sum the warp's 4 row groups (they share m).  Every lane of a group added the same
-    // p values to l, so after the sum any lane holds the warp's total.
+    // the 4 lanes of a quad summed different slots of the same head row
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+  }
+  __syncthreads();                                  // every warp (and every load) is done with the ring
+  if (warp < kWarps && hq < G) {
 #pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 8);
-      l[gg] += __shfl_xor_sync(0xffffffffu, l[gg], 16);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) {
-        float a = acc[gg][e];
-        a += __shfl_xor_sync(0xffffffffu, a, 8);
-        a += __shfl_xor_sync(0xffffffffu, a, 16);
-        acc[gg][e] = a;
-      }
+    for (int n = 0; n < NT; ++n) {
+      s_acc[warp][hq][8 * n + 2 * quad] = o[n][0];
+      s_acc[warp][hq][8 * n + 2 * quad + 1] = o[n][1];
     }
-    if (grp == 0) {
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-#pragma unroll
-        for (int e = 0; e < EPL; ++e) s_acc[warp][gg][(e >> 3) * 64 + sub * 8 + (e & 7)] = acc[gg][e];
-        if (sub == 0) {
-          s_ml[warp][gg][0] = m[gg];
-          s_ml[warp][gg][1] = l[gg];
-        }
-      }
+    if (quad == 0) {
+      s_ml[warp][hq][0] = m;
+      s_ml[warp][hq][1] = l;
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && s_abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 
   // ---- this block's partial: merge the warps ---------------------------------
   const int pairs = g.B * g.Hkv;
@@ -368,17 +369,34 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     ws_ml[(((int64_t)pair * nsplit + split) * G + gg) * 2 + 0] = M;
     ws_ml[(((int64_t)pair * nsplit + split) * G + gg) * 2 + 1] = L;
   }
-  __threadfence();
+  // The block's partial stores precede thread 0's acq_rel ticket (block barrier, then a
+  // release that is cumulative over them); the last block's loads follow its acquire.
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(tickets + pair, 1) == nsplit - 1;
+  if (threadIdx.x == 0) {
+    int prev;
+    asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(tickets + pair) : "memory");
+    s_last = prev == nsplit - 1;
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
   // ---- merge the splits (last block of this (b, kv head)) -------------------
-  // (m_s, l_s) of every used split and head into shared memory (the stage ring is free
-  // now), weights 2^(m_s - M) per head, then O over the splits.
+  // This thread's outputs e = threadIdx.x + i * blockDim.x load their first kPre split
+  // partials at once (one L2 round trip, in flight while the weights are formed); the
+  // (m_s, l_s) of every used split and head go to shared memory (the stage ring is free
+  // now), weights 2^(m_s - M) per head, then O = sum_s w_s O_s / sum_s w_s l_s.
+  constexpr int kOut = (G * D + kThreads - 1) / kThreads;         // outputs per thread
+  constexpr int kPre = 48 / kOut;                                  // splits prefetched per output
   const int used = min(nsplit, (len + share - 1) / share);       // later splits are empty
+  const float* ws_pair = ws_o + (int64_t)pair * nsplit * G * D;
+  float pre[kOut][kPre];
+#pragma unroll
+  for (int i = 0; i < kOut; ++i) {
+    const int e = threadIdx.x + i * kThreads;
+#pragma unroll
+    for (int k = 0; k < kPre; ++k)
+      pre[i][k] = (e < G * D && k < used) ? __ldcg(ws_pair + (int64_t)k * G * D + e) : 0.f;
+  }
   float* sw = reinterpret_cast<float*>(dsm);                     // [G][used] weights
   float* sl = sw + G * used;                                     // [G][used] sums
   for (int e = threadIdx.x; e < G * used; e += blockDim.x) {
@@ -407,17 +425,17 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+#pragma unroll
+  for (int i = 0; i < kOut; ++i) {
+    const int e = threadIdx.x + i * kThreads;
+    if (e >= G * D) break;
     const int gg = e / D, d = e - gg * D;
     const float* wrow = sw + gg * used;
-    const float* src = ws_o + (int64_t)pair * nsplit * G * D + (int64_t)gg * D + d;
     float o[4] = {0.f, 0.f, 0.f, 0.f};
-    int s = 0;
-    for (; s + 3 < used; s += 4) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) o[k] = fmaf(wrow[s + k], __ldcg(src + (int64_t)(s + k) * G * D), o[k]);
-    }
-    for (; s < used; ++s) o[0] = fmaf(wrow[s], __ldcg(src + (int64_t)s * G * D), o[0]);
+    for (int k = 0; k < kPre; ++k)
+      if (k < used) o[k & 3] = fmaf(wrow[k], pre[i][k], o[k & 3]);
+    for (int k = kPre; k < used; ++k) o[k & 3] = fmaf(wrow[k], __ldcg(ws_pair + (int64_t)k * G * D + e), o[k & 3]);
     store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, ((o[0] + o[1]) + (o[2] + o[3])) * s_inv[gg]);
   }
   if (threadIdx.x == 0) tickets[pair] = 0;
@@ -491,8 +509,8 @@ bool kvc_make_decode_maps(kvc_cache* c) {
   const kvc_config& g = c->cfg;
   const uint64_t batches = g.layout == KVC_PACKED ? 1 : (uint64_t)g.batch;
   const uint64_t cap = (uint64_t)c->cap;
-  return kvc_make_tile_map(&c->tm_dk, g.dtype, c->k, g.head_dim, g.kv_heads, cap, batches, kTile, KVC_BOX_ROWS) &&
-         kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, cap, batches, kTile, KVC_BOX_ROWS);
+  return kvc_make_tile_map(&c->tm_dk, g.dtype, c->k, g.head_dim, g.kv_heads, cap, batches, kTile, KVC_BOX_SW128) &&
+         kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, cap, batches, kTile, KVC_BOX_SW128);
 }
 
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s) {
