@@ -6,22 +6,19 @@
 // of their kv head's K and V (the repeat_interleave expansion of "Problem" is never
 // materialised).  The query is the newest token, so no mask applies.
 //
-// Grid (splits, Hkv, B).  Each block takes an equal share (at least kMinShare slots)
-// of the row's kv_len slots; the share is computed on the device from kv_len, so the
-// grid depends only on the shape and a captured graph replays at any length.
-// A producer warp streams the share through a ring of shared-memory stages with TMA
-// tile loads (112 whole rows of one kv head per box): one instruction moves 28 KB of K
-// or V, so the whole stream needs a few hundred copy requests per SM.  Seven consumer
-// warps take 16 slots of every 112-slot tile each, as 4 independent row groups whose
-// loads and dot products overlap and keep an online softmax (running
-// max m, sum l, accumulator) per q head; their states merge in shared memory into one
-// unnormalised partial (O_s, m_s, l_s) written to the workspace.  The last block of
-// each (b, kv head) to finish (a ticket counter in the workspace, left at zero for the
-// next call) merges the partials: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
-//
-// Lane mapping: 8 lanes per slot row, 4 rows per warp instruction; lane sub holds dims
-// {64 v + 8 sub + i : v < D/64, i < 8}, i.e. 16-byte chunk `sub` of each 64-dim half, so
-// the 8 lanes of a row read 128 contiguous bytes per load (one wavefront per row).
+// Grid (splits, Hkv, B); the grid depends only on the shape, so a captured graph
+// replays at any length.  A row's kv_len slots form tiles of kTile slots; each block
+// streams some of its (row, kv head)'s tiles: kStages fixed ones first, then tiles
+// claimed one at a time from a counter, so faster blocks take more.  A producer warp
+// moves each tile into a ring of shared-memory stages with TMA (128-byte-swizzled
+// boxes of 64 dims x kTile slots, K and V).  Seven consumer warps take 16 slots of
+// every tile each: S = Q K^T and O += P V run as warp-level m16n8k16 MMAs (the G q
+// heads of the group in M, padded to 16; slots or dims in N), with an online softmax
+// (running max m, sum l) per head row in between.  The warps' states merge in shared
+// memory into one unnormalised partial (O_s, m_s, l_s) per block, written to the
+// workspace; the last block of each (row, kv head) to finish (a ticket counter, left
+// at zero for the next call with the claim counter) merges the partials:
+// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 #include "kvc_internal.h"
 
 #include <cuda_bf16.h>
@@ -31,14 +28,9 @@
 
 namespace {
 
-// 8 warps per block: registers are split over the SM's 4 sub-partitions, so a block of
-// 8 warps may give each thread up to 255 registers (9 warps would cap it at 168).
 constexpr int kWarps = 7;                   // consumer warps
-constexpr int kGroups = 4;                  // row groups of 4 per consumer warp per tile
-constexpr int kRowsPerWarp = kGroups * 4;   // 16 rows of every tile per consumer warp
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
-constexpr int kMinShare = 64;               // fewest slots a block takes (short prefixes use few splits)
-constexpr int kTile = kWarps * kRowsPerWarp;  // 112 slots per stage (one TMA box of rows: 14 swizzle atoms)
+constexpr int kTile = kWarps * 16;          // 112 slots per stage, 16 per consumer warp
 constexpr int kStages = 4;                  // 4 x 56 KB in flight per SM (bandwidth x loaded latency)
 constexpr uint64_t kTimeoutNs = 500000000ull;
 
@@ -173,6 +165,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   __shared__ float s_ml[kWarps][G][2];
   __shared__ float s_inv[G];
   __shared__ int s_last, s_abort;
+  __shared__ int s_tile[kStages];    // tile index held by each stage, -1: no more tiles
 
   const int split = blockIdx.x, nsplit = gridDim.x;
   const int kvh = blockIdx.y, b = blockIdx.z;
@@ -185,12 +178,16 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   int row0 = 0, len = 0;
   if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;
 
-  int share = (len + nsplit - 1) / nsplit;
-  share = max(share, kMinShare);
-  share = (share + 15) & ~15;
-  const int t0 = split * share;
-  const int nt = max(0, min(len, t0 + share) - t0);
-  const int n_tiles = (nt + kTile - 1) / kTile;
+  // Tiles of kTile slots of this row: block `split` takes tiles split, split + nsplit, ...
+  // for its first kStages tiles, then claims tiles kStages * nsplit, ... one at a time
+  // from the (row, kv head) counter, so blocks that stream faster take more tiles.
+  const int n_row_tiles = (len + kTile - 1) / kTile;
+  const int pairs = g.B * g.Hkv;
+  const int pair = b * g.Hkv + kvh;
+  float* ws_o = ws;                                              // [pairs][nsplit][G][D]
+  float* ws_ml = ws + (int64_t)pairs * nsplit * G * D;           // [pairs][nsplit][G][2]
+  int* tickets = reinterpret_cast<int*>(ws_ml + (int64_t)pairs * nsplit * G * 2);  // [pairs]
+  int* claims = tickets + pairs;                                 // [pairs]
 
   if (threadIdx.x < kStages) {
     mbar_init(&full[threadIdx.x], 1);
@@ -206,18 +203,38 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (lane == 0) {
       const int kv_batch = g.layout == KVC_PACKED ? 0 : b;
       int issued = 0;
-      for (int t = 0; t < n_tiles; ++t) {
+      // tile t of this block: static for t < kStages, else claimed.  Claims are issued two
+      // tiles ahead, so that their round trips overlap the streaming of two tiles.
+      auto claim_for = [&](int t) {
+        return t < kStages ? split + t * nsplit : kStages * nsplit + atomicAdd(claims + pair, 1);
+      };
+      auto step = [&](int t, int tile) {
         const int st = t % kStages;
-        if (t >= kStages && !mbar_wait(&empty[st], ((t / kStages) - 1) & 1, abort)) break;
+        if (t >= kStages && !mbar_wait(&empty[st], ((t / kStages) - 1) & 1, abort)) return false;
+        if (tile >= n_row_tiles) {                       // no more tiles: tell the consumers
+          s_tile[st] = -1;
+          mbar_arrive(&full[st]);
+          return false;
+        }
+        s_tile[st] = tile;                               // published by the arrive below
         mbar_expect_tx(&full[st], SB);
         uint8_t* dst = dsm + st * SB;
-        const int row = row0 + t0 + t * kTile;
+        const int row = row0 + tile * kTile;
 #pragma unroll
         for (int h = 0; h < HB; ++h) {
           tma_load_4d(&tm_k, &full[st], dst + h * kHalfBytes, 64 * h, kvh, row, kv_batch);
           tma_load_4d(&tm_v, &full[st], dst + (HB + h) * kHalfBytes, 64 * h, kvh, row, kv_batch);
         }
         issued = t + 1;
+        return true;
+      };
+      static_assert(kStages >= 2, "the first two tiles are static");
+      int ca = claim_for(0), cb = claim_for(1);
+      for (int t = 0;; t += 2) {                         // claims are monotonic: none is skipped
+        if (!step(t, ca)) break;
+        ca = claim_for(t + 2);
+        if (!step(t + 1, cb)) break;
+        cb = claim_for(t + 3);
       }
       if (*abort) {   // let every load issued here land before the block releases its shared memory
         for (int t = max(0, issued - kStages); t < issued; ++t)
@@ -244,20 +261,23 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 
     const int r0 = warp * 16;                              // this warp's slots of every tile
-    for (int t = 0; t < n_tiles; ++t) {
+    for (int t = 0;; ++t) {
       const int st = t % kStages;
       if (!__all_sync(0xffffffffu, mbar_wait(&full[st], (t / kStages) & 1, abort))) break;
+      const int tile = s_tile[st];
+      if (tile < 0) break;
       const uint32_t kbase = smem_u32(dsm + st * SB);
       const uint32_t vbase = kbase + HB * kHalfBytes;
-      const int first = t * kTile + r0;                    // split-relative index of slot r0
-      if (first < nt) {
-        if (first + 16 > nt) {
+      const int first = tile * kTile + r0;                 // row index of slot r0
+      if (first < len) {
+        if (first + 16 > len) {
           // slots past the valid range may hold anything (NaN included): zero their V rows
           // so that P = 0 there contributes exactly nothing
           uint8_t* vrow = dsm + st * SB + HB * kHalfBytes;
           for (int e = lane; e < 16 * HB * 8; e += 32) {
             const int r = r0 + e / (HB * 8), h = (e / 8) % HB, c = e % 8;
-            if (t * kTile + r >= nt) *reinterpret_cast<uint4*>(vrow + h * kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            if (tile * kTile + r >= len)
+              *reinterpret_cast<uint4*>(vrow + h * kHalfBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // before TMA reuses the stage
           __syncwarp();
@@ -281,7 +301,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int sl = first + (e >> 1) * 8 + 2 * quad + (e & 1);
-          x[e] = sl < nt ? sc[e >> 1][e & 1] * scale_log2 : -INFINITY;
+          x[e] = sl < len ? sc[e >> 1][e & 1] * scale_log2 : -INFINITY;
         }
         float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
@@ -340,11 +360,6 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   __syncthreads();
 
   // ---- this block's partial: merge the warps ---------------------------------
-  const int pairs = g.B * g.Hkv;
-  const int pair = b * g.Hkv + kvh;
-  float* ws_o = ws;                                              // [pairs][nsplit][G][D]
-  float* ws_ml = ws + (int64_t)pairs * nsplit * G * D;           // [pairs][nsplit][G][2]
-  int* tickets = reinterpret_cast<int*>(ws_ml + (int64_t)pairs * nsplit * G * 2);  // [pairs]
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
     const int gg = e / D, d = e - gg * D;
     float M = -INFINITY;
@@ -387,7 +402,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   // now), weights 2^(m_s - M) per head, then O = sum_s w_s O_s / sum_s w_s l_s.
   constexpr int kOut = (G * D + kThreads - 1) / kThreads;         // outputs per thread
   constexpr int kPre = 48 / kOut;                                  // splits prefetched per output
-  const int used = min(nsplit, (len + share - 1) / share);       // later splits are empty
+  const int used = min(nsplit, n_row_tiles);                     // blocks past the tile count took none
   const float* ws_pair = ws_o + (int64_t)pair * nsplit * G * D;
   float pre[kOut][kPre];
 #pragma unroll
@@ -438,7 +453,10 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     for (int k = kPre; k < used; ++k) o[k & 3] = fmaf(wrow[k], __ldcg(ws_pair + (int64_t)k * G * D + e), o[k & 3]);
     store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, ((o[0] + o[1]) + (o[2] + o[3])) * s_inv[gg]);
   }
-  if (threadIdx.x == 0) tickets[pair] = 0;
+  if (threadIdx.x == 0) {           // every block of the pair is past both counters
+    tickets[pair] = 0;
+    claims[pair] = 0;
+  }
 }
 
 template <typename T, int D, int G>
@@ -500,7 +518,7 @@ bool kvc_decode_supported(const kvc_config& cfg) {
 size_t kvc_decode_workspace_bytes(const kvc_config& cfg, int splits) {
   const size_t pairs = (size_t)cfg.batch * cfg.kv_heads;
   const size_t G = cfg.heads / cfg.kv_heads;
-  return pairs * splits * G * (cfg.head_dim + 2) * 4 + pairs * 4;
+  return pairs * splits * G * (cfg.head_dim + 2) * 4 + pairs * 8;   // partials, tickets, tile claims
 }
 
 cudaError_t kvc_prepare_decode(kvc_cache* c) { return prepare_once(c); }
@@ -597,7 +615,7 @@ extern "C" int kvc_attend_decode_noalloc(const kvc_config* cfg, const void* k_st
   // the tickets sit after the partials; an earlier call with another shape may have
   // left partial data there
   const size_t pairs = (size_t)cfg->batch * cfg->kv_heads;
-  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - pairs * 4), 0, pairs * 4, s) != cudaSuccess)
+  if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - pairs * 8), 0, pairs * 8, s) != cudaSuccess)
     return KVC_ERR_CUDA;
   return kvc_launch_decode(&c, q, out, nullptr, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }
