@@ -276,9 +276,16 @@ int kvc_get_error(kvc_cache* c, void* stream, int32_t* bits) {
     return KVC_ERR_CUDA;
   if (bits != nullptr) *bits = word;
   if (word == 0) return KVC_OK;
-  if (cudaMemsetAsync(c->meta + KVC_META_ERR, 0, sizeof(int32_t), s) != cudaSuccess ||
-      cudaStreamSynchronize(s) != cudaSuccess)
-    return KVC_ERR_CUDA;
+  if (cudaMemsetAsync(c->meta + KVC_META_ERR, 0, sizeof(int32_t), s) != cudaSuccess) return KVC_ERR_CUDA;
+  if ((word & KVC_DEV_TIMEOUT) && c->ws != nullptr && c->dec_splits > 0) {
+    // a decode kernel that gave up may have left its ticket and tile-claim counters
+    // (the last 8 bytes per (row, kv head) of the workspace) off zero
+    const size_t raw = kvc_decode_workspace_bytes(c->cfg, c->dec_splits);
+    const size_t counters = (size_t)c->cfg.batch * c->cfg.kv_heads * 8;
+    if (cudaMemsetAsync(static_cast<unsigned char*>(c->ws) + (raw - counters), 0, counters, s) != cudaSuccess)
+      return KVC_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_ERR_CUDA;
   return KVC_ERR_DEVICE;
 }
 

@@ -109,7 +109,8 @@ enum {
 size_t kvc_meta_bytes(const kvc_config* cfg);
 
 /* Device scratch for the split-KV decode kernel (partial outputs and their
- * log-sum-exp terms, plus per-(row, kv-head) tickets that each call leaves at zero).
+ * log-sum-exp terms, plus per-(row, kv-head) ticket and tile-claim counters that
+ * each call leaves at zero).
  * Zero for a config with nothing to split.  Caller-allocated, passed to kvc_create. */
 size_t kvc_workspace_bytes(const kvc_config* cfg);
 
@@ -220,7 +221,9 @@ int kvc_reset(kvc_cache* c, int32_t row, void* stream);
 
 /* Synchronise `stream`, then return KVC_ERR_DEVICE if the device error word is
  * non-zero (its bits are stored in *bits when bits != NULL) and clear it; KVC_OK
- * otherwise. */
+ * otherwise.  When the word holds KVC_DEV_TIMEOUT, the decode kernel's ticket and
+ * tile-claim counters in the workspace are zeroed too, so the next attend starts
+ * clean. */
 int kvc_get_error(kvc_cache* c, void* stream, int32_t* bits);
 
 /* Free the host handle.  Device buffers stay with the caller. */
