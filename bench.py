@@ -285,20 +285,21 @@ def tc_traffic_per_launch(w, per_attend_kv):
 
 
 def cross_bench(kvc, peaks, reps=10, lq=None):
-    """Ragged cross-attention (2 CFG branches, H 40, D 128, 75600 padded queries, packed
-    text K/V by cu_seqlens): time per attend for the three length skews.  Q and O
-    traffic (3.1 GB) bounds it; the roofline time is max(bytes / HBM, flops / tensor)."""
+    """Ragged cross-attention (2 CFG branches, H 40, D 128, 75600 padded queries, text
+    K/V of at most 512 tokens per branch): time per attend for the three length skews in
+    two arms that compute the same result, packed K/V by cu_seqlens and a padded 512-slot
+    store with per-branch kv_len, plus the padded store attended unmasked (all 512 slots).
+    Q and O traffic (3.1 GB) bounds the first two; the roofline time is
+    max(bytes / HBM, flops / tensor)."""
     w = wl.CROSS
     B, H, D, Lq = w.batch, w.heads, w.head_dim, lq or wl.CROSS_LQ
+    L = wl.CROSS_LKV_MAX
     g = torch.Generator(device="cuda").manual_seed(w.seed)
     q = torch.randn(B, Lq, H, D, device="cuda", generator=g).bfloat16()
     out = torch.empty_like(q)
-    kv = torch.randn(B, wl.CROSS_LKV_MAX, H, D, device="cuda", generator=g).bfloat16()
-    res = {}
-    for name, lens in wl.CROSS_SKEWS.items():
-        c = kvc.KVCache(B, H, H, D, torch.bfloat16, "packed", capacity=2 * wl.CROSS_LKV_MAX)
-        c.set_lengths(cu_seqlens=torch.tensor(wl.seqlens_to_cu(lens), dtype=torch.int32, device="cuda"))
-        c.write(kv, kv)
+    kv = torch.randn(B, L, H, D, device="cuda", generator=g).bfloat16()
+
+    def timed(c, lens):
         for _ in range(3):
             c.attend(q, out)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -307,14 +308,26 @@ def cross_bench(kvc, peaks, reps=10, lq=None):
             c.attend(q, out)
         b.record()
         b.synchronize()
+        assert c.get_error() == 0
         t = a.elapsed_time(b) * 1e-3 / reps
         nbytes = 2 * q.numel() * 2 + sum(2 * n * H * D * 2 for n in lens)
         flops = sum(wl.attention_flops(Lq, n, H, D) for n in lens)
         roof = max(nbytes / (peaks["hbm"] * 1e9), flops / (peaks["bf16"] * 1e12))
-        res[name] = {"lens": list(lens), "ms": round(t * 1e3, 4), "GB/s": round(nbytes / t / 1e9, 1),
-                     "TFLOP/s": round(flops / t / 1e12, 1), "roofline_ms": round(roof * 1e3, 4),
-                     "frac": round(roof / t, 4)}
-        assert c.get_error() == 0
+        return {"lens": list(lens), "ms": round(t * 1e3, 4), "GB/s": round(nbytes / t / 1e9, 1),
+                "TFLOP/s": round(flops / t / 1e12, 1), "roofline_ms": round(roof * 1e3, 4),
+                "frac": round(roof / t, 4)}
+
+    padded = kvc.KVCache(B, H, H, D, torch.bfloat16, "linear", capacity=L)
+    padded.advance(n_tokens=L)
+    padded.write(kv, kv)
+    res = {"padded_512_unmasked": timed(padded, (L, L))}
+    for name, lens in wl.CROSS_SKEWS.items():
+        packed = kvc.KVCache(B, H, H, D, torch.bfloat16, "packed", capacity=2 * L)
+        packed.set_lengths(cu_seqlens=torch.tensor(wl.seqlens_to_cu(lens), dtype=torch.int32, device="cuda"))
+        packed.write(kv, kv)
+        padded.set_lengths(kv_len=torch.tensor(lens, dtype=torch.int32, device="cuda"))
+        res[name] = {"packed": timed(packed, lens), "kv_len": timed(padded, lens)}
+        packed.close()
     return res
 
 

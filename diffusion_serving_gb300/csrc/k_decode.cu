@@ -153,7 +153,7 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const T* __restrict__ q,
          T* __restrict__ out, int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2,
-         float* __restrict__ lse) {
+         float* __restrict__ lse, int fixed_tiles) {
   constexpr int HB = D / 64;         // 64-dim boxes per K (or V) tile
   constexpr int NT = D / 8;          // n-tiles of 8 dims in O
   constexpr uint32_t SB = stage_bytes<D>();
@@ -205,8 +205,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
       int issued = 0;
       // tile t of this block: static for t < kStages, else claimed.  Claims are issued two
       // tiles ahead, so that their round trips overlap the streaming of two tiles.
-      auto claim_for = [&](int t) {
-        return t < kStages ? split + t * nsplit : kStages * nsplit + atomicAdd(claims + pair, 1);
+      auto claim_for = [&](int t) {   // fixed_tiles: tile t is split + t * nsplit throughout
+        return t < kStages || fixed_tiles ? split + t * nsplit : kStages * nsplit + atomicAdd(claims + pair, 1);
       };
       auto step = [&](int t, int tile) {
         const int st = t % kStages;
@@ -460,30 +460,30 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s, bool prepare) {
+cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare) {
   constexpr size_t smem = dyn_smem_bytes<D>();
   if (prepare) return cudaFuncSetAttribute(k_decode<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
   return kvc_launch_pdl(k_decode<T, D, G>, grid, dim3(kThreads), smem, s, c->tm_dk, c->tm_dv, (const T*)q, (T*)out,
-                        c->meta, (float*)c->ws, g, c->scale * 1.4426950408889634f, lse);
+                        c->meta, (float*)c->ws, g, c->scale * 1.4426950408889634f, lse, fixed);
 }
 
 template <typename T, int D>
-cudaError_t launch_d(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s, bool prepare) {
+cudaError_t launch_d(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare) {
   switch (c->cfg.heads / c->cfg.kv_heads) {
-    case 1: return launch_dg<T, D, 1>(c, q, out, lse, s, prepare);
-    case 2: return launch_dg<T, D, 2>(c, q, out, lse, s, prepare);
-    case 4: return launch_dg<T, D, 4>(c, q, out, lse, s, prepare);
-    default: return launch_dg<T, D, 8>(c, q, out, lse, s, prepare);
+    case 1: return launch_dg<T, D, 1>(c, q, out, lse, fixed, s, prepare);
+    case 2: return launch_dg<T, D, 2>(c, q, out, lse, fixed, s, prepare);
+    case 4: return launch_dg<T, D, 4>(c, q, out, lse, fixed, s, prepare);
+    default: return launch_dg<T, D, 8>(c, q, out, lse, fixed, s, prepare);
   }
 }
 
 template <typename T>
-cudaError_t launch_t(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s, bool prepare) {
-  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, lse, s, prepare)
-                               : launch_d<T, 128>(c, q, out, lse, s, prepare);
+cudaError_t launch_t(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare) {
+  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, lse, fixed, s, prepare)
+                               : launch_d<T, 128>(c, q, out, lse, fixed, s, prepare);
 }
 
 // The decode kernels opt into their dynamic shared memory once per process and
@@ -501,8 +501,8 @@ cudaError_t prepare_once(kvc_cache* c) {
   const int gi = G == 1 ? 0 : G == 2 ? 1 : G == 4 ? 2 : 3;
   std::lock_guard<std::mutex> lock(g_prep_mu);
   if (g_prepared[dev][ti][di][gi]) return cudaSuccess;
-  e = ti == 0 ? launch_t<__half>(c, nullptr, nullptr, nullptr, 0, true)
-              : launch_t<__nv_bfloat16>(c, nullptr, nullptr, nullptr, 0, true);
+  e = ti == 0 ? launch_t<__half>(c, nullptr, nullptr, nullptr, 0, 0, true)
+              : launch_t<__nv_bfloat16>(c, nullptr, nullptr, nullptr, 0, 0, true);
   if (e == cudaSuccess) g_prepared[dev][ti][di][gi] = true;
   return e;
 }
@@ -531,11 +531,13 @@ bool kvc_make_decode_maps(kvc_cache* c) {
          kvc_make_tile_map(&c->tm_dv, g.dtype, c->v, g.head_dim, g.kv_heads, cap, batches, kTile, KVC_BOX_SW128);
 }
 
-cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s) {
+cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, bool fixed_tiles,
+                              cudaStream_t s) {
   const cudaError_t e = prepare_once(c);
   if (e != cudaSuccess) return e;
-  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, lse, s, false)
-                                 : launch_t<__nv_bfloat16>(c, q, out, lse, s, false);
+  const int fixed = fixed_tiles ? 1 : 0;
+  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, lse, fixed, s, false)
+                                 : launch_t<__nv_bfloat16>(c, q, out, lse, fixed, s, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -617,5 +619,5 @@ extern "C" int kvc_attend_decode_noalloc(const kvc_config* cfg, const void* k_st
   const size_t pairs = (size_t)cfg->batch * cfg->kv_heads;
   if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + (need - pairs * 8), 0, pairs * 8, s) != cudaSuccess)
     return KVC_ERR_CUDA;
-  return kvc_launch_decode(&c, q, out, nullptr, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
+  return kvc_launch_decode(&c, q, out, nullptr, false, s) == cudaSuccess ? KVC_OK : KVC_ERR_CUDA;
 }

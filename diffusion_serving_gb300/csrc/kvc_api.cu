@@ -59,13 +59,17 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int launched(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
 
+constexpr uint32_t kFlags = KVC_CAUSAL | KVC_KERNEL_SIMT | KVC_DETERMINISTIC;   // every attend flag
+
 // Kernel choice by shape only: fp32 (or the SIMT flag) -> fp32-FMA kernel; one query
 // token -> split-KV decode; bf16/fp16 with D = 128 -> tensor-core kernel; otherwise the
 // fp32-FMA kernel.
-int attend_impl(kvc_cache* c, const void* q, void* out, float* lse, int n_q, bool causal, bool simt,
-                cudaStream_t s) {
-  if (simt || c->cfg.dtype == KVC_F32) return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, lse, s));
-  if (n_q == 1 && c->dec_splits > 0) return launched(kvc_launch_decode(c, q, out, lse, s));
+int attend_impl(kvc_cache* c, const void* q, void* out, float* lse, int n_q, uint32_t flags, cudaStream_t s) {
+  const bool causal = (flags & KVC_CAUSAL) != 0;
+  if ((flags & KVC_KERNEL_SIMT) || c->cfg.dtype == KVC_F32)
+    return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, lse, s));
+  if (n_q == 1 && c->dec_splits > 0)
+    return launched(kvc_launch_decode(c, q, out, lse, (flags & KVC_DETERMINISTIC) != 0, s));
   if (c->tc_ok) return launched(kvc_launch_attn_tc(c, q, out, n_q, causal, lse, s));
   return launched(kvc_launch_attn_simt(c, q, out, n_q, causal, lse, s));
 }
@@ -224,20 +228,17 @@ int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_s
 
 int kvc_attend(kvc_cache* c, const void* q, void* out, int32_t n_q, uint32_t flags, void* stream) {
   if (c == nullptr || !q || !out || !aligned16(q) || !aligned16(out) || n_q < 1) return KVC_ERR_ARG;
-  if (flags & ~(uint32_t)(KVC_CAUSAL | KVC_KERNEL_SIMT)) return KVC_ERR_ARG;
-  const bool causal = (flags & KVC_CAUSAL) != 0;
-  if (causal && c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
-  cudaStream_t s = as_stream(stream);
-  return attend_impl(c, q, out, nullptr, n_q, causal, (flags & KVC_KERNEL_SIMT) != 0, s);
+  if (flags & ~kFlags) return KVC_ERR_ARG;
+  if ((flags & KVC_CAUSAL) && c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
+  return attend_impl(c, q, out, nullptr, n_q, flags, as_stream(stream));
 }
 
 int kvc_attend_lse(kvc_cache* c, const void* q, void* out, float* d_lse, int32_t n_q, uint32_t flags,
                    void* stream) {
   if (c == nullptr || !q || !out || !d_lse || !aligned16(q) || !aligned16(out) || n_q < 1) return KVC_ERR_ARG;
-  if (((uintptr_t)d_lse & 3u) != 0 || (flags & ~(uint32_t)(KVC_CAUSAL | KVC_KERNEL_SIMT))) return KVC_ERR_ARG;
-  const bool causal = (flags & KVC_CAUSAL) != 0;
-  if (causal && c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
-  return attend_impl(c, q, out, d_lse, n_q, causal, (flags & KVC_KERNEL_SIMT) != 0, as_stream(stream));
+  if (((uintptr_t)d_lse & 3u) != 0 || (flags & ~kFlags)) return KVC_ERR_ARG;
+  if ((flags & KVC_CAUSAL) && c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
+  return attend_impl(c, q, out, d_lse, n_q, flags, as_stream(stream));
 }
 
 int kvc_merge(int32_t dtype, int32_t n_rows, int32_t head_dim, const void* o_a, const float* lse_a, const void* o_b,

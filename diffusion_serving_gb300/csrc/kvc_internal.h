@@ -114,7 +114,7 @@ cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, in
 cudaError_t kvc_launch_roll(kvc_cache* c, void* scratch, cudaStream_t s);
 cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
                                  cudaStream_t s);
-cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, cudaStream_t s);
+cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, bool fixed_tiles, cudaStream_t s);
 cudaError_t kvc_prepare_decode(kvc_cache* c);
 bool kvc_decode_supported(const kvc_config& cfg);
 int kvc_internal_check_config(const kvc_config* cfg, int* cap);

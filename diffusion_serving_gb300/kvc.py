@@ -22,7 +22,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "kvc.h")
 
 F32, F16, BF16 = 0, 1, 2
 LINEAR, CIRCULAR, PACKED = 0, 1, 2
-CAUSAL, KERNEL_SIMT = 1, 256
+CAUSAL, KERNEL_SIMT, DETERMINISTIC = 1, 256, 512
 OK, ERR_ARG, ERR_UNSUPPORTED, ERR_RANGE, ERR_CUDA, ERR_DEVICE = 0, -1, -2, -3, -4, -5
 DEV_BAD_SLOT, DEV_BAD_KVLEN, DEV_BAD_CUSEQ, DEV_OVERFLOW, DEV_NO_CHUNK, DEV_TIMEOUT, DEV_BAD_POS = 1, 2, 4, 8, 16, 32, 64
 META_ROW0 = 4

@@ -96,8 +96,12 @@ enum {
 enum {
   KVC_CAUSAL = 1,           /* LINEAR only: query i at position kv_len - n_q + i sees
                                keys at positions <= its own [PFX "Change"]          */
-  KVC_KERNEL_SIMT = 256     /* run the fp32-FMA kernel for any dtype (a cross-check
+  KVC_KERNEL_SIMT = 256,    /* run the fp32-FMA kernel for any dtype (a cross-check
                                of the tensor-core and decode kernels)               */
+  KVC_DETERMINISTIC = 512   /* decode (n_q == 1): give every block a fixed set of tiles.
+                               Without it, rows longer than 4 x the split count spread
+                               their later tiles to whichever blocks stream fastest, so
+                               the last bits of the result can vary between calls   */
 };
 
 /* Meta block: int32 words, device memory owned by the caller.
@@ -182,7 +186,8 @@ int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_s
  * Valid slots: [0, kv_len_b) for LINEAR and CIRCULAR, [cu_b, cu_{b+1}) for PACKED;
  * nothing past them is read into the result [PFX "Change"].
  *  q (device [B, n_q, H, D]), out (device, same shape and dtype).
- *  flags: KVC_CAUSAL (LINEAR only, else KVC_ERR_UNSUPPORTED), KVC_KERNEL_SIMT.
+ *  flags: KVC_CAUSAL (LINEAR only, else KVC_ERR_UNSUPPORTED), KVC_KERNEL_SIMT,
+ *  KVC_DETERMINISTIC.
  *  A row whose kv_len is outside [1, cap] at run time gets KVC_DEV_BAD_KVLEN and
  *  its output is left unwritten. */
 int kvc_attend(kvc_cache* c, const void* q, void* out, int32_t n_q, uint32_t flags,
