@@ -7,9 +7,10 @@
 // materialised).  The query is the newest token, so no mask applies.
 //
 // Grid (splits, Hkv, B); the grid depends only on the shape, so a captured graph
-// replays at any length.  A row's kv_len slots form tiles of kTile slots; each block
-// streams some of its (row, kv head)'s tiles: kStages fixed ones first, then tiles
-// claimed one at a time from a counter, so faster blocks take more.  A producer warp
+// replays at any length.  A row's kv_len slots form tiles of kTile slots.  A row of at
+// most kSoloTiles tiles is streamed by one block, which writes the output directly.
+// Otherwise each block streams some of its (row, kv head)'s tiles: kStages fixed ones
+// first, then tiles claimed one at a time from a counter, so faster blocks take more.  A producer warp
 // moves each tile into a ring of shared-memory stages with TMA (128-byte-swizzled
 // boxes of 64 dims x kTile slots, K and V).  Seven consumer warps take 16 slots of
 // every tile each: S = Q K^T and O += P V run as warp-level m16n8k16 MMAs (the G q
@@ -31,6 +32,7 @@ namespace {
 constexpr int kWarps = 7;                   // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
 constexpr int kTile = kWarps * 16;          // 112 slots per stage, 16 per consumer warp
+constexpr int kSoloTiles = 6;               // rows of at most this many tiles: one block, no split merge
 constexpr int kStages = 4;                  // 4 x 56 KB in flight per SM (bandwidth x loaded latency)
 constexpr uint64_t kTimeoutNs = 500000000ull;
 
@@ -163,7 +165,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   // per-warp partial accumulators [kWarps][G][D]: the stage ring, once every warp is past it
   float (*s_acc)[G][D] = reinterpret_cast<float (*)[G][D]>(dsm);
   __shared__ float s_ml[kWarps][G][2];
-  __shared__ float s_inv[G];
+  __shared__ float s_inv[G], s_max[G];
   __shared__ int s_last, s_abort;
   __shared__ int s_tile[kStages];    // tile index held by each stage, -1: no more tiles
 
@@ -182,6 +184,11 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   // for its first kStages tiles, then claims tiles kStages * nsplit, ... one at a time
   // from the (row, kv head) counter, so blocks that stream faster take more tiles.
   const int n_row_tiles = (len + kTile - 1) / kTile;
+  // A short row is streamed by block 0 of its (row, kv head) alone, which writes the
+  // output directly: for a few tiles the split merge (partials, ticket, last-block
+  // merge) costs more than one block streaming them.  Uniform per block.
+  const bool solo = n_row_tiles <= kSoloTiles;
+  if (solo && split != 0) return;
   const int pairs = g.B * g.Hkv;
   const int pair = b * g.Hkv + kvh;
   float* ws_o = ws;                                              // [pairs][nsplit][G][D]
@@ -206,6 +213,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
       // tile t of this block: static for t < kStages, else claimed.  Claims are issued two
       // tiles ahead, so that their round trips overlap the streaming of two tiles.
       auto claim_for = [&](int t) {   // fixed_tiles: tile t is split + t * nsplit throughout
+        if (solo) return t;
         return t < kStages || fixed_tiles ? split + t * nsplit : kStages * nsplit + atomicAdd(claims + pair, 1);
       };
       auto step = [&](int t, int tile) {
@@ -358,8 +366,36 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     }
   }
   __syncthreads();
+  if (threadIdx.x == 0 && s_abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 
   // ---- this block's partial: merge the warps ---------------------------------
+  if (solo) {   // the whole row: normalise and write the output
+    if (threadIdx.x < G) {
+      const int gg = threadIdx.x;
+      float M = -INFINITY, L = 0.f;
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][gg][0]);
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = s_ml[w][gg][0];
+        if (mw != -INFINITY) L = fmaf(ex2(mw - M), s_ml[w][gg][1], L);
+      }
+      s_max[gg] = M;
+      s_inv[gg] = 1.f / L;
+      if (lse != nullptr) lse[(int64_t)b * g.H + kvh * G + gg] = (M + log2f(L)) * 0.6931471805599453f;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+      const int gg = e / D, d = e - gg * D;
+      const float M = s_max[gg];
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = s_ml[w][gg][0];
+        if (mw != -INFINITY) a = fmaf(ex2(mw - M), s_acc[w][gg][d], a);
+      }
+      store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, a * s_inv[gg]);
+    }
+    return;
+  }
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
     const int gg = e / D, d = e - gg * D;
     float M = -INFINITY;
