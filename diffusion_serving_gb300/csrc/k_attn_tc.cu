@@ -14,8 +14,9 @@
 // K/V tile it loads.  The kernel is persistent: one CTA per SM walks the items.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q tiles once, then K and V tiles of 128 slots into a
 //               two-stage ring (128B-swizzled boxes of 64 dims x 128 slots).
-//   warp 1      TMEM owner and MMA issuer: S = Q K^T (A, B from shared memory) and
-//               O += P V (P from TMEM, V from shared memory), fp32 accumulators in TMEM.
+//   warps 1, 2  MMA issuers, one per query tile (warp 1 also owns TMEM): S = Q K^T
+//               (A, B from shared memory) and O += P V (P from TMEM, V from shared
+//               memory), fp32 accumulators in TMEM.
 //   warps 4-7   softmax of tile A, one query row per thread: S row from TMEM, online
 //               max / exp2 / sum, P written back to TMEM over S, O rescaled in TMEM
 //               when the row max grows by more than 2^8, final O / l to global.
@@ -23,9 +24,13 @@
 // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512); P_X occupies the
 // first 64 columns of S_X as packed 16-bit pairs.
 //
-// MMA order per K/V tile j (one issuing thread): PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1).
-// The commit that signals "S_A(j+1) ready" also covers PV_A(j), so when the softmax
-// warps see S_A(j+1) the O_A accumulator is stable and may be rescaled.
+// MMA order per K/V tile j: PV_A(j), QK_A(j+1) from warp 1 and PV_B(j), QK_B(j+1) from
+// warp 2, with B's PV(j) issued after A's and A's PV(j+1) after B's PV(j) (the order of
+// a single issuer, at half-group granularity, so that the tiles' softmaxes alternate).
+// A single thread issues MMAs at most every ~100 cycles while the tensor pipe retires
+// one per 64, so two issuing warps overlap one tile's QK with the other's PV.  The
+// commit that signals "S_X(j+1) ready" also covers PV_X(j) (same thread, in order), so
+// when the softmax warps see S_X(j+1) the O_X accumulator is stable and may be rescaled.
 //
 // Every mbarrier wait is bounded (0.5 s of %globaltimer); on expiry the kernel records
 // KVC_DEV_TIMEOUT, drains its own TMA loads and MMAs, frees TMEM and returns, and CTAs
@@ -59,8 +64,10 @@ struct Smem {
   uint64_t q_full, q_free;
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t v_ready[kStages];   // V tile with its invalid rows zeroed (warp 1 -> warp 2)
+  uint64_t tok[2];             // issue order: tok[t] = issuer t has issued its PV of tile j
   uint64_t s_full[2], p_ready[2], o_done[2];
-  uint64_t drain;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -373,19 +380,23 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
-    mbar_init(&sm.q_free, 1);
+    mbar_init(&sm.q_free, 2);   // both issuers' last QK of the item
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
-      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.k_empty[s], 2);   // QK of both query tiles
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.v_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 2);   // PV of both query tiles
+      mbar_init(&sm.v_ready[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
       mbar_init(&sm.p_ready[t], kBM / 32);   // one arrival per softmax warp
       mbar_init(&sm.o_done[t], 1);
     }
-    mbar_init(&sm.drain, 1);
+    mbar_init(&sm.tok[0], 1);
+    mbar_init(&sm.tok[1], 1);
+    mbar_init(&sm.drain[0], 1);
+    mbar_init(&sm.drain[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -446,24 +457,29 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           mbar_wait(&sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer (lane 0) + V tail zeroing (whole warp) ----------------
+  } else if (warp == 1 || warp == 2) {
+    // ---------------- MMA issuers: warp 1 for query tile A, warp 2 for tile B ----------------
+    // Each issues its tile's chain PV(j), QK(j + 1) from one thread (in order, so QK(j + 1)
+    // overwrites S only after PV(j) read P from it); two issuing warps on different
+    // sub-partitions feed the tensor pipe faster than one.  Warp 1 also zeroes the
+    // invalid rows of a last V tile and then signals v_ready for warp 2.
+    const int t = warp - 1;
     constexpr uint32_t kIdQK = idesc_f16(kBf16 ? 1u : 0u, 0);
     constexpr uint32_t kIdPV = idesc_f16(kBf16 ? 1u : 0u, 1);
-    const uint32_t s_col[2] = {0u, 128u}, o_col[2] = {256u, 384u};
-    auto issue_qk = [&](int t, int s) {
+    const uint32_t s_col = t ? 128u : 0u, o_col = t ? 384u : 256u;
+    auto issue_qk = [&](int s) {
       const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[s]);
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-        mma_ss(tmem + s_col[t], sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdQK, kk > 0);
+        mma_ss(tmem + s_col, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdQK, kk > 0);
       }
     };
-    auto issue_pv = [&](int t, int s, int j) {
+    auto issue_pv = [&](int s, int j) {
       const uint32_t va = smem_u32(sm.v[s]);
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_ts(tmem + o_col[t], tmem + s_col[t] + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
+        mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
                (j > 0 || kk > 0) ? 1u : 0u);
     };
     int T = 0, n_items_done = 0;
@@ -478,60 +494,61 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        issue_qk(0, s0);
-        mma_commit(&sm.s_full[0]);
-        issue_qk(1, s0);
-        mma_commit(&sm.s_full[1]);
+        issue_qk(s0);
+        mma_commit(&sm.s_full[t]);
         mma_commit(&sm.k_empty[s0]);
         if (I.n_tiles == 1) mma_commit(&sm.q_free);
       }
       __syncwarp();
       for (int j = 0; ok && j < I.n_tiles; ++j) {
         const int Tj = T + j, s = Tj % kStages, u = Tj / kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
-        if (!ok) break;
-        const int rem = I.kv_end - j * kBN;
-        if (rem < kBN) {
-          // slots past the valid range may hold anything (NaN included): zero those V rows
-          // so that P = 0 there contributes exactly nothing
-          for (int e = lane; e < (kBN - rem) * 2 * 8; e += 32) {
-            const int r = rem + e / 16, half = (e / 8) & 1, c = e & 7;
-            *reinterpret_cast<uint4*>(sm.v[s] + half * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        if (t == 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
+          if (!ok) break;
+          const int rem = I.kv_end - j * kBN;
+          if (rem < kBN) {
+            // slots past the valid range may hold anything (NaN included): zero those V rows
+            // so that P = 0 there contributes exactly nothing
+            for (int e = lane; e < (kBN - rem) * 2 * 8; e += 32) {
+              const int r = rem + e / 16, half = (e / 8) & 1, c = e & 7;
+              *reinterpret_cast<uint4*>(sm.v[s] + half * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async();
           }
-          fence_proxy_async();
           __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.v_ready[s]);
+        } else {
+          ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_ready[s], u & 1, abort));
+          if (!ok) break;
         }
         const bool more = j + 1 < I.n_tiles;
         const int s1 = (Tj + 1) % kStages, u1 = (Tj + 1) / kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[0], Tj & 1, abort));
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[t], Tj & 1, abort));
+        if (!ok) break;
+        // keep the single-issuer order PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) at half-group
+        // granularity: B's PV(j) after A issued PV(j), A's PV(j) after B issued PV(j - 1),
+        // so that the two tiles stay half a period apart and their softmaxes alternate
+        if (t == 1) ok = __all_sync(0xffffffffu, mbar_wait(&sm.tok[0], Tj & 1, abort));
+        else if (Tj > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.tok[1], (Tj - 1) & 1, abort));
         if (!ok) break;
         tc_fence_after();
-        if (lane == 0) issue_pv(0, s, j);
+        if (lane == 0) {
+          issue_pv(s, j);
+          mma_commit(&sm.v_empty[s]);
+          mbar_arrive(&sm.tok[t]);
+        }
         if (more) {
           ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s1], u1 & 1, abort));
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            issue_qk(0, s1);
-            mma_commit(&sm.s_full[0]);
-          }
-        } else if (lane == 0) {
-          mma_commit(&sm.o_done[0]);
-        }
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[1], Tj & 1, abort));
-        if (!ok) break;
-        tc_fence_after();
-        if (lane == 0) {
-          issue_pv(1, s, j);
-          mma_commit(&sm.v_empty[s]);
-          if (more) {
-            issue_qk(1, s1);
-            mma_commit(&sm.s_full[1]);
+            issue_qk(s1);
+            mma_commit(&sm.s_full[t]);
             mma_commit(&sm.k_empty[s1]);
             if (j + 2 == I.n_tiles) mma_commit(&sm.q_free);   // that was this item's last QK
-          } else {
-            mma_commit(&sm.o_done[1]);
           }
+        } else if (lane == 0) {
+          mma_commit(&sm.o_done[t]);
         }
         __syncwarp();
       }
@@ -540,8 +557,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     }
     if (*abort && lane == 0) {
       // drain: all MMAs issued by this thread complete before TMEM is released
-      mma_commit(&sm.drain);
-      mbar_wait(&sm.drain, 0, abort, false);
+      mma_commit(&sm.drain[t]);
+      mbar_wait(&sm.drain[t], 0, abort, false);
     }
     __syncwarp();
   } else if (warp >= 4) {
