@@ -40,6 +40,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 namespace {
 
 constexpr int kD = 128;
@@ -260,13 +262,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 // Row max of the 128 scores a thread holds, over columns < valid when kMask (eight
 // independent chains of 3-input maxima so that the reduction is not one long
 // dependency).
-template <bool kMask>
+template <bool kMask, int kChunks>
 __device__ __forceinline__ float row_max(const uint32_t* sr, int valid) {
   float mx[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) mx[k] = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 128; i += 2) {
+  for (int i = 0; i < 32 * kChunks; i += 2) {
     float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
     if (kMask) {
       x0 = i < valid ? x0 : -INFINITY;
@@ -277,15 +279,23 @@ __device__ __forceinline__ float row_max(const uint32_t* sr, int valid) {
   return fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
 }
 
-// p = 2^(s * c - m) for the 128 columns (0 past `valid` when kMask), packed as 16-bit
-// pairs over the first 64 TMEM columns of the row's S; returns the row sum of p.
-// Pairs of columns go through the packed fp32x2 FMA / add.
-template <bool kBf16, bool kMask>
+// p = 2^(s * c - m) for the first 32 * kChunks columns (0 past `valid` when kMask),
+// packed as 16-bit pairs over the first 64 TMEM columns of the row's S; the P of the
+// chunks past kChunks is stored as 0 (the PV MMA reads all 128).  Returns the row sum of
+// p.  Pairs of columns go through the packed fp32x2 FMA / add.
+template <bool kBf16, bool kMask, int kChunks>
 __device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, float c, float m_use, uint32_t s_addr) {
   const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
   float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  if (kChunks < 4) {
+    uint32_t zero[16];
 #pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
+    for (int i = 0; i < 16; ++i) zero[i] = 0u;
+#pragma unroll
+    for (int q4 = kChunks; q4 < 4; ++q4) tmem_st16(s_addr + q4 * 16, zero);
+  }
+#pragma unroll
+  for (int q4 = 0; q4 < kChunks; ++q4) {
     uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -585,43 +595,64 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], Tj & 1, abort));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[128];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tmem_ld32(s_addr + q4 * 32, sr + q4 * 32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) reg_fence32(sr + q4 * 32);
         int valid = I.kv_end - j * kBN;                          // columns < valid are slots in range
         if (p.causal) valid = min(valid, qpos - j * kBN + 1);
-        const bool full = !p.causal && I.kv_end - j * kBN >= kBN;   // uniform: no column masked
-        const float mx = full ? row_max<false>(sr, valid) : row_max<true>(sr, valid);
-        const float m_tile = mx * c;
-        bool rescale = m_tile > m_ref + kRescaleThreshold;
-        const float m_new = rescale ? m_tile : m_ref;
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        if (__any_sync(0xffffffffu, rescale) && j > 0) {
-          const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
-#pragma unroll 1
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint32_t orow[32];
-            tmem_ld32(o_addr + q4 * 32, orow);
-            tmem_ld_wait();
-            reg_fence32(orow);
+        // One pass over the tile's S row: kChunks 32-column chunks hold slots in range
+        // (fewer than 4 only on a short last tile without the causal mask, where
+        // `valid` is the same for every row); kMask masks columns past `valid`.
+        auto tile = [&](auto chunks, auto mask) {
+          constexpr int kC = decltype(chunks)::value;
+          constexpr bool kM = decltype(mask)::value;
+          uint32_t sr[128];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[i]), __uint_as_float(orow[i + 1])),
-                                          make_float2(alpha, alpha));
-              orow[i] = __float_as_uint(y.x);
-              orow[i + 1] = __float_as_uint(y.y);
+          for (int q4 = 0; q4 < kC; ++q4) tmem_ld32(s_addr + q4 * 32, sr + q4 * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q4 = 0; q4 < kC; ++q4) reg_fence32(sr + q4 * 32);
+          const float m_tile = row_max<kM, kC>(sr, valid) * c;
+          bool rescale = m_tile > m_ref + kRescaleThreshold;
+          const float m_new = rescale ? m_tile : m_ref;
+          const float m_use = m_new == -INFINITY ? 0.f : m_new;
+          if (__any_sync(0xffffffffu, rescale) && j > 0) {
+            const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t orow[32];
+              tmem_ld32(o_addr + q4 * 32, orow);
+              tmem_ld_wait();
+              reg_fence32(orow);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[i]), __uint_as_float(orow[i + 1])),
+                                            make_float2(alpha, alpha));
+                orow[i] = __float_as_uint(y.x);
+                orow[i + 1] = __float_as_uint(y.y);
+              }
+              tmem_st32(o_addr + q4 * 32, orow);
             }
-            tmem_st32(o_addr + q4 * 32, orow);
+            tmem_st_wait();
+            l *= alpha;
           }
-          tmem_st_wait();
-          l *= alpha;
+          m_ref = m_new;
+          l += exp_pack_store<kBf16, kM, kC>(sr, valid, c, m_use, s_addr);
+        };
+        using C1 = std::integral_constant<int, 1>;
+        using C2 = std::integral_constant<int, 2>;
+        using C3 = std::integral_constant<int, 3>;
+        using C4 = std::integral_constant<int, 4>;
+        using Masked = std::true_type;
+        if (p.causal || valid >= kBN) {   // causal: `valid` differs between rows
+          if (!p.causal) tile(C4{}, std::false_type{});
+          else tile(C4{}, Masked{});
+        } else if (valid <= 32) {
+          tile(C1{}, Masked{});
+        } else if (valid <= 64) {
+          tile(C2{}, Masked{});
+        } else if (valid <= 96) {
+          tile(C3{}, Masked{});
+        } else {
+          tile(C4{}, Masked{});
         }
-        m_ref = m_new;
-        l += full ? exp_pack_store<kBf16, false>(sr, valid, c, m_use, s_addr)
-                  : exp_pack_store<kBf16, true>(sr, valid, c, m_use, s_addr);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
