@@ -669,30 +669,37 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       // conflict-free) -> one TMA store per 32 columns; rows past n_q are clipped by the map
       const int grow = I.row_a + t * kBM + quad * 32;    // first query row of this warp
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t orow[32];
-        tmem_ld32(o_addr + q4 * 32, orow);
+      for (int q2 = 0; q2 < 2; ++q2) {                  // 64 columns per TMEM round trip
+        uint32_t orow[64];
+        tmem_ld32(o_addr + q2 * 64, orow);
+        tmem_ld32(o_addr + q2 * 64 + 32, orow + 32);
         tmem_ld_wait();
         reg_fence32(orow);
-        uint32_t pk[16];
+        reg_fence32(orow + 32);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[2 * i]), __uint_as_float(orow[2 * i + 1])),
-                                      make_float2(inv, inv));
-          pk[i] = pack2<kBf16>(y.x, y.y);
-        }
-        uint8_t* buf = stage + (q4 & 1) * kStageBytes;
-        if (lane == 0) bulk_wait_read1();                // the store that last read buf is done with it
-        __syncwarp();
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int q4 = 2 * q2 + c2;
+          const uint32_t* oc = orow + 32 * c2;
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
-              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_4d(&tm_o, buf, q4 * 32, I.h, grow, I.b);
-          bulk_commit();
+          for (int i = 0; i < 16; ++i) {
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(oc[2 * i]), __uint_as_float(oc[2 * i + 1])),
+                                        make_float2(inv, inv));
+            pk[i] = pack2<kBf16>(y.x, y.y);
+          }
+          uint8_t* buf = stage + c2 * kStageBytes;
+          if (lane == 0) bulk_wait_read1();              // the store that last read buf is done with it
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&tm_o, buf, q4 * 32, I.h, grow, I.b);
+            bulk_commit();
+          }
         }
       }
       // O of this item has been read: the issuer may overwrite it once this warp's next
