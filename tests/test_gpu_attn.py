@@ -328,3 +328,29 @@ def test_causal_prefill(n_q, kv_len):
                      q_pos0=kv_len - n_q)
     assert_close(out[0], ref, "causal")
     assert cache.get_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_last_tile_chunk_boundaries(dtype):
+    """Rows whose last K/V tile ends on and next to every 32-column chunk boundary: the
+    tensor-core kernel then reads 1, 2, 3 or 4 chunks of that tile's S row and stores a
+    zero P for the rest.  Slots past kv_len hold NaN; the result must equal the oracle
+    and the run with a clean tail, bit for bit."""
+    lens = [1, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129, 161, 255, 256]
+    B, H, D, cap, n_q = len(lens), 2, 128, 384, 96
+    cache = kvc.KVCache(B, H, H, D, dtype, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(17)
+    cache.k_store.normal_(generator=g)
+    cache.v_store.normal_(generator=g)
+    cache.set_lengths(kv_len=torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    q = torch.randn(B, n_q, H, D, device="cuda", generator=g).to(dtype)
+    clean = cache.attend(q)
+    for b, n in enumerate(lens):
+        cache.k_store[b, n:] = float("nan")
+        cache.v_store[b, n:] = float("nan")
+    dirty = cache.attend(q)
+    assert torch.equal(bits(clean), bits(dirty))
+    for b, n in enumerate(lens):
+        ref = orc.attend(to64(q[b]), to64(cache.k_store[b, :n]), to64(cache.v_store[b, :n]))
+        assert_close(dirty[b], ref, f"kv_len {n}")
+    assert cache.get_error() == 0
