@@ -526,10 +526,29 @@ def ours(args):
         torch.cuda.synchronize()
         barrier(dist)
         e2e_t = max_over_ranks(a.elapsed_time(b) * 1e-3, dist)
+        # the host link alone, for reading the number above: one chunk's inputs up, one
+        # output down, pinned buffers, nothing else running
+        hq, hk, hv = host[0]
+        q, k, v = dev[0]
+        a.record(comp)
+        for _ in range(3):
+            q.copy_(hq, non_blocking=True)
+            k.copy_(hk, non_blocking=True)
+            v.copy_(hv, non_blocking=True)
+        b.record(comp)
+        b.synchronize()
+        up = 3 * sum(t.numel() * t.element_size() for t in host[0]) / (a.elapsed_time(b) * 1e-3) / 1e9
+        a.record(comp)
+        for _ in range(3):
+            out_host[0].copy_(dev_out[0], non_blocking=True)
+        b.record(comp)
+        b.synchronize()
+        down = 3 * out_host[0].numel() * out_host[0].element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
         result["e2e"] = {"value": round(world * step_flops * args.steps / e2e_t / 1e12, 2), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": round(e2e_t / args.steps * 1e3, 3),
-                         "pipelining": "inputs up and outputs down on two copy streams, overlapping compute"}
+                         "pipelining": "inputs up and outputs down on two copy streams, overlapping compute",
+                         "host_link_GB/s": {"h2d": round(up, 1), "d2h": round(down, 1)}}
     if rank == 0:
         tf, dt, nrows = cpu_oracle_sample(w)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
