@@ -265,20 +265,29 @@ def decode_bench(kvc, peaks, per_graph=64, replays=5):
     return res
 
 
+def kernel_code_sha256(path):
+    """sha256 of a CUDA source with its // comments and blank lines removed: the code a
+    capture was taken of (comment edits do not change the kernel)."""
+    import hashlib
+    import re
+    with open(path) as f:
+        text = f.read()
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in lines if ln).encode()).hexdigest()
+
+
 def tc_traffic_per_launch(w, per_attend_kv):
     """DRAM bytes per attend launch, from the committed capture of the chunk kernel:
     the capture's DRAM / algorithmic ratio times this workload's average algorithmic
-    bytes (Q and O once, valid K/V once).  None when the kernel source changed since."""
-    import hashlib
+    bytes (Q and O once, valid K/V once).  None when the kernel code changed since."""
     path = os.path.join(ROOT, "profiles", "k_attn_tc_traffic.json")
     src = os.path.join(ROOT, "diffusion_serving_gb300", "csrc", "k_attn_tc.cu")
     if not (os.path.exists(path) and os.path.exists(src)):
         return None
     with open(path) as f:
         cap = json.load(f)
-    with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != cap["kernel_source_sha256"]:
-            return None
+    if kernel_code_sha256(src) != cap.get("kernel_code_sha256"):
+        return None
     qo = 2 * w.batch * w.chunk * w.heads * w.head_dim * 2
     kv = [2 * w.batch * n * w.kv_heads * w.head_dim * 2 for n in per_attend_kv]
     return round(cap["dram_over_algorithmic"] * (qo + float(np.mean(kv))))

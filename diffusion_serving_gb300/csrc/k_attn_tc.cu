@@ -10,16 +10,20 @@
 // "pass only active KV cache prefix to SDPA", "Change"); with KVC_CAUSAL the query
 // at absolute position kv_len - n_q + i sees slots <= that position (same section).
 //
-// Work item = two 128-row query tiles (A and B) of one (batch row, q head), sharing every
-// K/V tile it loads.  The kernel is persistent: one CTA per SM walks the items.  Warp roles (384 threads):
-//   warp 0      TMA producer: Q tiles once, then K and V tiles of 128 slots into a
-//               two-stage ring (128B-swizzled boxes of 64 dims x 128 slots).
+// Work item = two 128-row query tiles (A and B) of one (batch row, q head), sharing
+// every K/V tile it loads.  The kernel is persistent: one CTA per SM walks the items.
+// Warp roles (384 threads):
+//   warp 0      TMA producer: the item's Q tiles, then K and V tiles of 128 slots into
+//               two-stage rings (128B-swizzled boxes of 64 dims x 128 slots).
 //   warps 1, 2  MMA issuers, one per query tile (warp 1 also owns TMEM): S = Q K^T
 //               (A, B from shared memory) and O += P V (P from TMEM, V from shared
 //               memory), fp32 accumulators in TMEM.
 //   warps 4-7   softmax of tile A, one query row per thread: S row from TMEM, online
 //               max / exp2 / sum, P written back to TMEM over S, O rescaled in TMEM
-//               when the row max grows by more than 2^8, final O / l to global.
+//               when the row max grows by more than 2^8; at the end O / l goes to
+//               global memory through 64-byte-swizzled shared staging and TMA stores.
+//               A short last tile (no causal mask) skips its 32-column chunks past the
+//               valid slots.
 //   warps 8-11  the same for tile B.
 // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512); P_X occupies the
 // first 64 columns of S_X as packed 16-bit pairs.

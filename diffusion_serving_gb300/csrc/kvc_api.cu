@@ -102,13 +102,11 @@ bool kvc_make_tile_map(CUtensorMap* m, int dtype, const void* base, int D, uint6
   if (enc == nullptr || (dtype != KVC_BF16 && dtype != KVC_F16)) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, d1, d2, d3};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2ull, d1 * D * 2ull, d2 * d1 * D * 2ull};
-  const cuuint32_t inner = box == KVC_BOX_ROWS ? (cuuint32_t)D : box == KVC_BOX_SW64 ? 32u : 64u;
+  const cuuint32_t inner = box == KVC_BOX_SW64 ? 32u : 64u;
   const cuuint32_t boxdim[4] = {inner, 1, box_rows, 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUtensorMapDataType t = dtype == KVC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  const CUtensorMapSwizzle sw = box == KVC_BOX_ROWS   ? CU_TENSOR_MAP_SWIZZLE_NONE
-                                : box == KVC_BOX_SW64 ? CU_TENSOR_MAP_SWIZZLE_64B
-                                                      : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle sw = box == KVC_BOX_SW64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return enc(m, t, 4, const_cast<void*>(base), dims, strides, boxdim, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

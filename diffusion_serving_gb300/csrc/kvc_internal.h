@@ -127,10 +127,9 @@ cudaError_t kvc_launch_merge(int dtype, int rows, int head_dim, const void* oa, 
 bool kvc_tc_supported(const kvc_config& cfg);
 bool kvc_tc_make_kv_maps(kvc_cache* c);
 // Box shapes of a 4-D TMA map over a 16-bit tensor [d3][d2][d1][D] (D = 64 or 128):
-//   KVC_BOX_SW128: 64 x 1 x box_rows x 1 elements, 128-byte swizzle (tcgen05 operand tiles)
-//   KVC_BOX_ROWS:  D x 1 x box_rows x 1, unswizzled (whole rows)
+//   KVC_BOX_SW128: 64 x 1 x box_rows x 1 elements, 128-byte swizzle (MMA operand tiles)
 //   KVC_BOX_SW64:  32 x 1 x box_rows x 1, 64-byte swizzle (output staging of 32 columns)
-enum kvc_box { KVC_BOX_SW128 = 0, KVC_BOX_ROWS = 1, KVC_BOX_SW64 = 2 };
+enum kvc_box { KVC_BOX_SW128 = 0, KVC_BOX_SW64 = 2 };
 // False if the driver entry point is missing or the encoding is rejected.
 bool kvc_make_tile_map(CUtensorMap* m, int dtype, const void* base, int D, uint64_t d1, uint64_t d2, uint64_t d3,
                        uint32_t box_rows, kvc_box box = KVC_BOX_SW128);
