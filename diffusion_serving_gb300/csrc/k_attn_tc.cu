@@ -1,4 +1,7 @@
 // Tensor-core chunk attention for bf16 / fp16, D = 128 (sm_103a: tcgen05 + TMEM + TMA).
+// Two kernels share the helpers below: k_attn_tc (a pair of query tiles per item, for
+// stores of at most kShortKv slots per row) and k_attn_1q (one query tile per item with
+// S and O double-buffered in TMEM, for longer stores); the launcher picks by shape.
 //
 // Computes, for every query row of a chunk, softmax(scale * q K^T) V over the row's
 // valid slots in physical order: [0, kv_len) of a LINEAR or CIRCULAR store (the
@@ -53,6 +56,7 @@ constexpr int kBM = 128;            // query rows per tile
 constexpr int kBN = 128;            // slots per K/V tile
 constexpr int kStages = 2;
 constexpr int kThreads = 384;
+constexpr int kShortKv = 1024;      // stores of at most this many slots per row: the query-tile-pair kernel
 constexpr uint32_t kBoxBytes = 64 * 2 * 128;         // 64 dims x 128 rows, 16-bit
 constexpr uint32_t kTileBytes = 2 * kBoxBytes;       // 128 dims
 constexpr uint32_t kStageBytes = 32 * 32 * 2;        // 32 rows x 32 dims, 16-bit
@@ -726,11 +730,406 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 }
 
 // ---- host side ----------------------------------------------------------------
+// ---- one query tile per item: S and O double-buffered in TMEM ----------------------
+// Work item = one 128-row query tile of one (batch row, q head); items run tile-fastest,
+// so the CTAs working at once share a (row, head)'s K/V tiles through L2.  TMEM holds
+// two S buffers and two O buffers (4 x 128 columns), so
+//   * QK of K/V tile j + 1 runs while the softmax works on S(j) (no tile ping-pong is
+//     needed to keep the tensor pipe busy),
+//   * the QK and PV MMAs come from two warps on different sub-partitions: S(j + 2)
+//     reuses S(j)'s columns only after PV(j) read P(j) from them (s_free),
+//   * O alternates between items, so the next item's PV can run while the epilogue
+//     reads the previous item's O (o_free).
+// Warps (256 threads): 0 TMA producer (Q double-buffered per item, K and V two-stage
+// rings), 1 QK issuer and TMEM owner, 2 PV issuer (and V-tail zeroing), 4-7 softmax and
+// epilogue of the tile's 128 rows (warp & 3 = TMEM lane quadrant).
+constexpr int kThreads1 = 256;
+
+struct Smem1 {
+  uint8_t q[2][kTileBytes];             // Q tile per item, double-buffered
+  uint8_t k[kStages][kTileBytes];
+  uint8_t v[kStages][kTileBytes];
+  uint8_t o_stage[4][2][kStageBytes];   // output staging per softmax warp (64-byte swizzle)
+  uint64_t q_full[2], q_free[2];
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], p_ready[2], s_free[2];   // per S buffer
+  uint64_t o_done[2], o_free[2];               // per O buffer
+  uint64_t drain[2];
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Smem1) + 1024 <= 232448, "shared memory above the 227 KB a block may opt into");
+static_assert(offsetof(Smem1, o_stage) % 1024 == 0, "staging buffers must keep the swizzle phase of their address");
+
+__device__ __forceinline__ bool item_geom1(int item, int qtiles, const TcParams& p, int32_t* meta, RowCache& rc,
+                                           Item* it) {
+  const kvc_geom& g = p.g;
+  const int qt = item % qtiles, bh = item / qtiles;
+  it->h = bh % g.H;
+  it->b = bh / g.H;
+  it->kvh = it->h / (g.H / g.Hkv);
+  it->row_a = qt * kBM;
+  if (it->b != rc.b) {
+    rc.b = it->b;
+    rc.ok = kvc_row_range(meta, g, it->b, &rc.row0, &rc.len, meta + KVC_META_ERR);
+  }
+  if (!rc.ok) return false;
+  const int len = rc.len;
+  it->row0 = rc.row0;
+  it->kv_batch = g.layout == KVC_PACKED ? 0 : it->b;
+  it->qpos0 = len - p.n_q;
+  it->kv_end = len;
+  if (p.causal) {
+    const int last_row = min(it->row_a + kBM, p.n_q) - 1;
+    it->kv_end = max(1, min(len, it->qpos0 + last_row + 1));
+  }
+  it->n_tiles = (it->kv_end + kBN - 1) / kBN;
+  return true;
+}
+
+template <bool kBf16>
+__global__ void __launch_bounds__(kThreads1, 1)
+k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+          int32_t* __restrict__ meta, TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem1& sm = *reinterpret_cast<Smem1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const kvc_geom& g = p.g;
+  const int qtiles = (p.n_q + kBM - 1) / kBM;
+  const int n_items = g.B * g.H * qtiles;
+
+  if (threadIdx.x == 0)
+    sm.abort = (*reinterpret_cast<volatile int32_t*>(meta + KVC_META_ERR) & KVC_DEV_TIMEOUT) ? 1 : 0;
+  __syncthreads();
+  if (sm.abort) return;
+  volatile int* abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.q_full[b], 1);
+      mbar_init(&sm.q_free[b], 1);
+      mbar_init(&sm.s_full[b], 1);
+      mbar_init(&sm.p_ready[b], kBM / 32);   // one arrival per softmax warp
+      mbar_init(&sm.s_free[b], 1);
+      mbar_init(&sm.o_done[b], 1);
+      mbar_init(&sm.o_free[b], kBM / 32);
+      mbar_init(&sm.drain[b], 1);
+    }
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int T = 0, n = 0;
+      RowCache rc;
+      int k_issued = 0, v_issued = 0, q_issued = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        Item I;
+        if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
+        const int qb = n & 1;
+        if (n >= 2 && !mbar_wait(&sm.q_free[qb], ((n >> 1) - 1) & 1, abort)) break;   // item n - 2's last QK
+        mbar_expect_tx(&sm.q_full[qb], kTileBytes);
+        for (int half = 0; half < 2; ++half)
+          tma_load_4d(&tm_q, &sm.q_full[qb], sm.q[qb] + half * kBoxBytes, half * 64, I.h, I.row_a, I.b);
+        q_issued = n + 1;
+        for (int j = 0; j < I.n_tiles; ++j) {
+          const int Tj = T + j, s = Tj % kStages, u = Tj / kStages;
+          const int row = I.row0 + j * kBN;
+          if (Tj >= kStages && !mbar_wait(&sm.k_empty[s], (u - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.k_full[s], kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(&tm_k, &sm.k_full[s], sm.k[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
+          k_issued = Tj + 1;
+          if (Tj >= kStages && !mbar_wait(&sm.v_empty[s], (u - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&sm.v_full[s], kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(&tm_v, &sm.v_full[s], sm.v[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
+          v_issued = Tj + 1;
+        }
+        T += I.n_tiles;
+        ++n;
+      }
+      if (*abort) {
+        // drain: every load this thread issued lands before the CTA's shared memory is released
+        for (int m = max(0, q_issued - 2); m < q_issued; ++m) mbar_wait(&sm.q_full[m & 1], (m >> 1) & 1, abort, false);
+        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
+          mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, abort, false);
+        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
+          mbar_wait(&sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- QK issuer: S(T) = Q K(T)^T into S buffer T % 2 ----------------
+    constexpr uint32_t kIdQK = idesc_f16(kBf16 ? 1u : 0u, 0);
+    int T = 0, n = 0;
+    RowCache rc;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      Item I;
+      if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
+      const int qb = n & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (n >> 1) & 1, abort));
+      for (int j = 0; ok && j < I.n_tiles; ++j) {
+        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj & 1;
+        // K(T) landed, and S buffer sb is free: PV(T - 2) read its P
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s], u & 1, abort) &&
+                                         (Tj < 2 || mbar_wait(&sm.s_free[sb], ((Tj >> 1) - 1) & 1, abort)));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t qa = smem_u32(sm.q[qb]), ka = smem_u32(sm.k[s]);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+            mma_ss(tmem + sb * 128u, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdQK, kk > 0);
+          }
+          mma_commit(&sm.s_full[sb]);
+          mma_commit(&sm.k_empty[s]);
+          if (j + 1 == I.n_tiles) mma_commit(&sm.q_free[qb]);
+        }
+        __syncwarp();
+      }
+      T += I.n_tiles;
+      ++n;
+    }
+    if (*abort && lane == 0) {
+      mma_commit(&sm.drain[0]);
+      mbar_wait(&sm.drain[0], 0, abort, false);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---------------- PV issuer: O(item) += P(T) V(T) ----------------
+    constexpr uint32_t kIdPV = idesc_f16(kBf16 ? 1u : 0u, 1);
+    int T = 0, n = 0;
+    RowCache rc;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      Item I;
+      if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
+      const int ob = n & 1;
+      // O buffer ob is free once the epilogue of item n - 2 has read it
+      ok = __all_sync(0xffffffffu, n < 2 || mbar_wait(&sm.o_free[ob], ((n >> 1) - 1) & 1, abort));
+      for (int j = 0; ok && j < I.n_tiles; ++j) {
+        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
+        if (!ok) break;
+        const int rem = I.kv_end - j * kBN;
+        if (rem < kBN) {
+          // slots past the valid range may hold anything (NaN included): zero those V rows
+          // so that P = 0 there contributes exactly nothing
+          for (int e = lane; e < (kBN - rem) * 2 * 8; e += 32) {
+            const int r = rem + e / 16, half = (e / 8) & 1, c = e & 7;
+            *reinterpret_cast<uint4*>(sm.v[s] + half * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+          __syncwarp();
+        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[sb], (Tj >> 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t va = smem_u32(sm.v[s]);
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + 256u + ob * 128u, tmem + sb * 128u + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024),
+                   kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&sm.s_free[sb]);
+          mma_commit(&sm.v_empty[s]);
+          if (j + 1 == I.n_tiles) mma_commit(&sm.o_done[ob]);
+        }
+        __syncwarp();
+      }
+      T += I.n_tiles;
+      ++n;
+    }
+    if (*abort && lane == 0) {
+      mma_commit(&sm.drain[1]);
+      mbar_wait(&sm.drain[1], 0, abort, false);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------- softmax and epilogue (one query row per thread) ----------------
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quad * 32) << 16);
+    const float c = p.scale_log2;
+    uint8_t* const stage = sm.o_stage[quad][0];
+    int T = 0, n = 0;
+    RowCache rc;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      Item I;
+      if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
+      const int ob = n & 1;
+      const uint32_t o_addr = lane_addr + 256u + ob * 128u;
+      const int row = I.row_a + r;
+      const int qpos = I.qpos0 + row;
+      float m_ref = -INFINITY, l = 0.f;
+      for (int j = 0; j < I.n_tiles; ++j) {
+        const int Tj = T + j, sb = Tj & 1;
+        const uint32_t s_addr = lane_addr + sb * 128u;
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (Tj >> 1) & 1, abort));
+        if (!ok) break;
+        tc_fence_after();
+        int valid = I.kv_end - j * kBN;
+        if (p.causal) valid = min(valid, qpos - j * kBN + 1);
+        auto tile = [&](auto chunks, auto mask) {
+          constexpr int kC = decltype(chunks)::value;
+          constexpr bool kM = decltype(mask)::value;
+          uint32_t sr[128];
+#pragma unroll
+          for (int q4 = 0; q4 < kC; ++q4) tmem_ld32(s_addr + q4 * 32, sr + q4 * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q4 = 0; q4 < kC; ++q4) reg_fence32(sr + q4 * 32);
+          const float m_tile = row_max<kM, kC>(sr, valid) * c;
+          bool rescale = m_tile > m_ref + kRescaleThreshold;
+          const float m_new = rescale ? m_tile : m_ref;
+          const float m_use = m_new == -INFINITY ? 0.f : m_new;
+          if (__any_sync(0xffffffffu, rescale) && j > 0) {
+            // O may be rescaled only once PV(T - 1) has finished accumulating into it
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_free[(Tj - 1) & 1], ((Tj - 1) >> 1) & 1, abort))) return;
+            tc_fence_after();
+            const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
+#pragma unroll 1
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t orow[32];
+              tmem_ld32(o_addr + q4 * 32, orow);
+              tmem_ld_wait();
+              reg_fence32(orow);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[i]), __uint_as_float(orow[i + 1])),
+                                            make_float2(alpha, alpha));
+                orow[i] = __float_as_uint(y.x);
+                orow[i + 1] = __float_as_uint(y.y);
+              }
+              tmem_st32(o_addr + q4 * 32, orow);
+            }
+            tmem_st_wait();
+            l *= alpha;
+          }
+          m_ref = m_new;
+          l += exp_pack_store<kBf16, kM, kC>(sr, valid, c, m_use, s_addr);
+        };
+        using C1 = std::integral_constant<int, 1>;
+        using C2 = std::integral_constant<int, 2>;
+        using C3 = std::integral_constant<int, 3>;
+        using C4 = std::integral_constant<int, 4>;
+        using Masked = std::true_type;
+        if (p.causal || valid >= kBN) {
+          if (!p.causal) tile(C4{}, std::false_type{});
+          else tile(C4{}, Masked{});
+        } else if (valid <= 32) {
+          tile(C1{}, Masked{});
+        } else if (valid <= 64) {
+          tile(C2{}, Masked{});
+        } else if (valid <= 96) {
+          tile(C3{}, Masked{});
+        } else {
+          tile(C4{}, Masked{});
+        }
+        if (*abort) {
+          ok = false;
+          break;
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_ready[sb]);
+      }
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[ob], (n >> 1) & 1, abort));
+      if (!ok) break;
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (p.lse != nullptr && row < p.n_q)   // m_ref and l are in the exp2 domain of scale * q.k
+        p.lse[((int64_t)I.b * p.n_q + row) * g.H + I.h] =
+            l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      const int grow = I.row_a + quad * 32;    // first query row of this warp
+#pragma unroll 1
+      for (int q2 = 0; q2 < 2; ++q2) {                  // 64 columns per TMEM round trip
+        uint32_t orow[64];
+        tmem_ld32(o_addr + q2 * 64, orow);
+        tmem_ld32(o_addr + q2 * 64 + 32, orow + 32);
+        tmem_ld_wait();
+        reg_fence32(orow);
+        reg_fence32(orow + 32);
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int q4 = 2 * q2 + c2;
+          const uint32_t* oc = orow + 32 * c2;
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 y = __fmul2_rn(make_float2(__uint_as_float(oc[2 * i]), __uint_as_float(oc[2 * i + 1])),
+                                        make_float2(inv, inv));
+            pk[i] = pack2<kBf16>(y.x, y.y);
+          }
+          uint8_t* buf = stage + c2 * kStageBytes;
+          if (lane == 0) bulk_wait_read1();
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&tm_o, buf, q4 * 32, I.h, grow, I.b);
+            bulk_commit();
+          }
+        }
+      }
+      // every TMEM read of O(ob) is complete: item n + 2's PV may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+      T += I.n_tiles;
+      ++n;
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && sm.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
+}
+
 bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t d1, uint64_t d2, uint64_t d3) {
   return kvc_make_tile_map(m, dtype, base, kD, d1, d2, d3, 128);
 }
 
 size_t smem_bytes() { return sizeof(Smem) + 1024; }
+size_t smem_bytes1() { return sizeof(Smem1) + 1024; }
 
 }  // namespace
 
@@ -749,6 +1148,11 @@ bool kvc_tc_make_kv_maps(kvc_cache* c) {
     return false;
   if (cudaFuncSetAttribute(k_attn_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return false;
+  const size_t smem1 = smem_bytes1();
+  if (cudaFuncSetAttribute(k_attn_1q<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) != cudaSuccess)
+    return false;
+  if (cudaFuncSetAttribute(k_attn_1q<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1) != cudaSuccess)
+    return false;
   return true;
 }
 
@@ -766,12 +1170,27 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
   p.causal = causal ? 1 : 0;
   p.scale_log2 = c->scale * 1.4426950408889634f;
   p.lse = lse;
-  const int64_t items = (int64_t)((n_q + 2 * kBM - 1) / (2 * kBM)) * cfg.heads * cfg.batch;
+  // Kernel by shape (a captured graph stays valid at any length): stores whose rows hold
+  // at most kShortKv slots (the whole store for PACKED) give items of a few K/V tiles,
+  // where the pair kernel's eight softmax warps keep the per-item chain short; longer
+  // stores run the one-tile kernel, whose double-buffered S keeps the tensor pipe fed
+  // (measured crossover between 512 and 1024 slots).
+  if (c->cap <= kShortKv) {
+    const int64_t items = (int64_t)((n_q + 2 * kBM - 1) / (2 * kBM)) * cfg.heads * cfg.batch;
+    if (items > INT32_MAX) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)(items < c->num_sms ? items : c->num_sms));
+    if (cfg.dtype == KVC_BF16)
+      k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
+    else
+      k_attn_tc<false><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
+    return cudaGetLastError();
+  }
+  const int64_t items = (int64_t)((n_q + kBM - 1) / kBM) * cfg.heads * cfg.batch;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   dim3 grid((unsigned)(items < c->num_sms ? items : c->num_sms));    // persistent: one CTA per SM
   if (cfg.dtype == KVC_BF16)
-    k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
+    k_attn_1q<true><<<grid, kThreads1, smem_bytes1(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
   else
-    k_attn_tc<false><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
+    k_attn_1q<false><<<grid, kThreads1, smem_bytes1(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
   return cudaGetLastError();
 }

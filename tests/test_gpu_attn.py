@@ -331,13 +331,14 @@ def test_causal_prefill(n_q, kv_len):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
-def test_last_tile_chunk_boundaries(dtype):
+@pytest.mark.parametrize("cap", [384, 2048])   # short stores: query-tile-pair kernel; long: one-tile kernel
+def test_last_tile_chunk_boundaries(dtype, cap):
     """Rows whose last K/V tile ends on and next to every 32-column chunk boundary: the
-    tensor-core kernel then reads 1, 2, 3 or 4 chunks of that tile's S row and stores a
+    tensor-core kernels then read 1, 2, 3 or 4 chunks of that tile's S row and store a
     zero P for the rest.  Slots past kv_len hold NaN; the result must equal the oracle
     and the run with a clean tail, bit for bit."""
     lens = [1, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129, 161, 255, 256]
-    B, H, D, cap, n_q = len(lens), 2, 128, 384, 96
+    B, H, D, n_q = len(lens), 2, 128, 300
     cache = kvc.KVCache(B, H, H, D, dtype, "linear", capacity=cap)
     g = torch.Generator(device="cuda").manual_seed(17)
     cache.k_store.normal_(generator=g)
