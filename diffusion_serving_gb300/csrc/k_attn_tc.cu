@@ -730,19 +730,19 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 }
 
 // ---- host side ----------------------------------------------------------------
-// ---- one query tile per item: S and O double-buffered in TMEM ----------------------
+// ---- one query tile per item: S triple-buffered in TMEM -----------------------------
 // Work item = one 128-row query tile of one (batch row, q head); items run tile-fastest,
 // so the CTAs working at once share a (row, head)'s K/V tiles through L2.  TMEM holds
-// two S buffers and two O buffers (4 x 128 columns), so
-//   * QK of K/V tile j + 1 runs while the softmax works on S(j) (no tile ping-pong is
-//     needed to keep the tensor pipe busy),
-//   * the QK and PV MMAs come from two warps on different sub-partitions: S(j + 2)
-//     reuses S(j)'s columns only after PV(j) read P(j) from them (s_free),
-//   * O alternates between items, so the next item's PV can run while the epilogue
-//     reads the previous item's O (o_free).
+// three S buffers and O (4 x 128 columns), and the QK and PV MMAs come from two warps on
+// different sub-partitions.  S(j + 3) reuses S(j)'s columns once PV(j) has read P(j)
+// from them (s_free), so the loop softmax(j) -> PV(j) -> QK(j + 3) -> softmax(j + 3)
+// spans three tiles and the softmax warps, not the MMA issue, set the pace.  O is read
+// by the epilogue before the next item's first PV (o_free): one bubble per item, which
+// is small on the long rows this kernel is for.
 // Warps (256 threads): 0 TMA producer (Q double-buffered per item, K and V two-stage
 // rings), 1 QK issuer and TMEM owner, 2 PV issuer (and V-tail zeroing), 4-7 softmax and
 // epilogue of the tile's 128 rows (warp & 3 = TMEM lane quadrant).
+constexpr int kSBufs = 3;
 constexpr int kThreads1 = 256;
 
 struct Smem1 {
@@ -753,8 +753,8 @@ struct Smem1 {
   uint64_t q_full[2], q_free[2];
   uint64_t k_full[kStages], k_empty[kStages];
   uint64_t v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], p_ready[2], s_free[2];   // per S buffer
-  uint64_t o_done[2], o_free[2];               // per O buffer
+  uint64_t s_full[kSBufs], p_ready[kSBufs], s_free[kSBufs];   // per S buffer
+  uint64_t o_done, o_free;
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
@@ -810,13 +810,15 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.q_full[b], 1);
       mbar_init(&sm.q_free[b], 1);
+      mbar_init(&sm.drain[b], 1);
+    }
+    for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_ready[b], kBM / 32);   // one arrival per softmax warp
       mbar_init(&sm.s_free[b], 1);
-      mbar_init(&sm.o_done[b], 1);
-      mbar_init(&sm.o_free[b], kBM / 32);
-      mbar_init(&sm.drain[b], 1);
     }
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.o_free, kBM / 32);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
@@ -894,10 +896,10 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       const int qb = n & 1;
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (n >> 1) & 1, abort));
       for (int j = 0; ok && j < I.n_tiles; ++j) {
-        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj & 1;
-        // K(T) landed, and S buffer sb is free: PV(T - 2) read its P
+        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj % kSBufs;
+        // K(T) landed, and S buffer sb is free: PV(T - 3) read its P
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s], u & 1, abort) &&
-                                         (Tj < 2 || mbar_wait(&sm.s_free[sb], ((Tj >> 1) - 1) & 1, abort)));
+                                         (Tj < kSBufs || mbar_wait(&sm.s_free[sb], (Tj / kSBufs - 1) & 1, abort)));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -930,11 +932,10 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       Item I;
       if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
-      const int ob = n & 1;
-      // O buffer ob is free once the epilogue of item n - 2 has read it
-      ok = __all_sync(0xffffffffu, n < 2 || mbar_wait(&sm.o_free[ob], ((n >> 1) - 1) & 1, abort));
+      // O is free once the epilogue of item n - 1 has read it
+      ok = __all_sync(0xffffffffu, n < 1 || mbar_wait(&sm.o_free, (n - 1) & 1, abort));
       for (int j = 0; ok && j < I.n_tiles; ++j) {
-        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj & 1;
+        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj % kSBufs;
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
         if (!ok) break;
         const int rem = I.kv_end - j * kBN;
@@ -948,18 +949,18 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           fence_proxy_async();
           __syncwarp();
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[sb], (Tj >> 1) & 1, abort));
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_ready[sb], (Tj / kSBufs) & 1, abort));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
           const uint32_t va = smem_u32(sm.v[s]);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tmem + 256u + ob * 128u, tmem + sb * 128u + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024),
-                   kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(tmem + 384u, tmem + sb * 128u + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
+                   (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&sm.s_free[sb]);
           mma_commit(&sm.v_empty[s]);
-          if (j + 1 == I.n_tiles) mma_commit(&sm.o_done[ob]);
+          if (j + 1 == I.n_tiles) mma_commit(&sm.o_done);
         }
         __syncwarp();
       }
@@ -984,15 +985,14 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       Item I;
       if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
-      const int ob = n & 1;
-      const uint32_t o_addr = lane_addr + 256u + ob * 128u;
+      const uint32_t o_addr = lane_addr + 384u;
       const int row = I.row_a + r;
       const int qpos = I.qpos0 + row;
       float m_ref = -INFINITY, l = 0.f;
       for (int j = 0; j < I.n_tiles; ++j) {
-        const int Tj = T + j, sb = Tj & 1;
+        const int Tj = T + j, sb = Tj % kSBufs;
         const uint32_t s_addr = lane_addr + sb * 128u;
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (Tj >> 1) & 1, abort));
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (Tj / kSBufs) & 1, abort));
         if (!ok) break;
         tc_fence_after();
         int valid = I.kv_end - j * kBN;
@@ -1012,7 +1012,8 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           const float m_use = m_new == -INFINITY ? 0.f : m_new;
           if (__any_sync(0xffffffffu, rescale) && j > 0) {
             // O may be rescaled only once PV(T - 1) has finished accumulating into it
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_free[(Tj - 1) & 1], ((Tj - 1) >> 1) & 1, abort))) return;
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_free[(Tj - 1) % kSBufs], ((Tj - 1) / kSBufs) & 1, abort)))
+              return;
             tc_fence_after();
             const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
 #pragma unroll 1
@@ -1062,7 +1063,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_ready[sb]);
       }
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[ob], (n >> 1) & 1, abort));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done, n & 1, abort));
       if (!ok) break;
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -1104,10 +1105,10 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           }
         }
       }
-      // every TMEM read of O(ob) is complete: item n + 2's PV may overwrite it
+      // every TMEM read of O is complete: item n + 1's first PV may overwrite it
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sm.o_free[ob]);
+      if (lane == 0) mbar_arrive(&sm.o_free);
       T += I.n_tiles;
       ++n;
     }
