@@ -739,9 +739,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 // spans three tiles and the softmax warps, not the MMA issue, set the pace.  O is read
 // by the epilogue before the next item's first PV (o_free): one bubble per item, which
 // is small on the long rows this kernel is for.
-// Warps (256 threads): 0 TMA producer (Q double-buffered per item, K and V two-stage
-// rings), 1 QK issuer and TMEM owner, 2 PV issuer (and V-tail zeroing), 4-7 softmax and
-// epilogue of the tile's 128 rows (warp & 3 = TMEM lane quadrant).
+// Warps (256 threads): 0 TMA producer of Q (double-buffered per item) and K, 3 TMA
+// producer of V (two-stage rings each), 1 QK issuer and TMEM owner, 2 PV issuer (and
+// V-tail zeroing), 4-7 softmax and epilogue of the tile's 128 rows (warp & 3 = TMEM lane
+// quadrant).
 constexpr int kSBufs = 3;
 constexpr int kThreads1 = 256;
 
@@ -836,41 +837,40 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == 3) {
+    // ---------------- TMA producers: warp 0 Q and K, warp 3 V ----------------
+    // (two threads, so that a K load never queues behind a V load waiting for a PV)
     if (lane == 0) {
+      const bool kq = warp == 0;
       int T = 0, n = 0;
       RowCache rc;
-      int k_issued = 0, v_issued = 0, q_issued = 0;
+      int issued = 0, q_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         Item I;
         if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
-        const int qb = n & 1;
-        if (n >= 2 && !mbar_wait(&sm.q_free[qb], ((n >> 1) - 1) & 1, abort)) break;   // item n - 2's last QK
-        mbar_expect_tx(&sm.q_full[qb], kTileBytes);
-        for (int half = 0; half < 2; ++half)
-          tma_load_4d(&tm_q, &sm.q_full[qb], sm.q[qb] + half * kBoxBytes, half * 64, I.h, I.row_a, I.b);
-        q_issued = n + 1;
+        if (kq) {
+          const int qb = n & 1;
+          if (n >= 2 && !mbar_wait(&sm.q_free[qb], ((n >> 1) - 1) & 1, abort)) break;   // item n - 2's last QK
+          mbar_expect_tx(&sm.q_full[qb], kTileBytes);
+          for (int half = 0; half < 2; ++half)
+            tma_load_4d(&tm_q, &sm.q_full[qb], sm.q[qb] + half * kBoxBytes, half * 64, I.h, I.row_a, I.b);
+          q_issued = n + 1;
+        }
+        const CUtensorMap* tm = kq ? &tm_k : &tm_v;
         for (int j = 0; j < I.n_tiles; ++j) {
           const int Tj = T + j, s = Tj % kStages, u = Tj / kStages;
-          const int row = I.row0 + j * kBN;
-          if (Tj >= kStages && !mbar_wait(&sm.k_empty[s], (u - 1) & 1, abort)) {
+          uint64_t* empty = kq ? &sm.k_empty[s] : &sm.v_empty[s];
+          uint64_t* full = kq ? &sm.k_full[s] : &sm.v_full[s];
+          uint8_t* dst = kq ? sm.k[s] : sm.v[s];
+          if (Tj >= kStages && !mbar_wait(empty, (u - 1) & 1, abort)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&sm.k_full[s], kTileBytes);
+          mbar_expect_tx(full, kTileBytes);
           for (int half = 0; half < 2; ++half)
-            tma_load_4d(&tm_k, &sm.k_full[s], sm.k[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
-          k_issued = Tj + 1;
-          if (Tj >= kStages && !mbar_wait(&sm.v_empty[s], (u - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&sm.v_full[s], kTileBytes);
-          for (int half = 0; half < 2; ++half)
-            tma_load_4d(&tm_v, &sm.v_full[s], sm.v[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
-          v_issued = Tj + 1;
+            tma_load_4d(tm, full, dst + half * kBoxBytes, half * 64, I.kvh, I.row0 + j * kBN, I.kv_batch);
+          issued = Tj + 1;
         }
         T += I.n_tiles;
         ++n;
@@ -878,10 +878,8 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       if (*abort) {
         // drain: every load this thread issued lands before the CTA's shared memory is released
         for (int m = max(0, q_issued - 2); m < q_issued; ++m) mbar_wait(&sm.q_full[m & 1], (m >> 1) & 1, abort, false);
-        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
-          mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, abort, false);
-        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
-          mbar_wait(&sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
+        for (int j = max(0, issued - kStages); j < issued; ++j)
+          mbar_wait(kq ? &sm.k_full[j % kStages] : &sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
       }
     }
   } else if (warp == 1) {
