@@ -16,8 +16,8 @@
 // Work item = two 128-row query tiles (A and B) of one (batch row, q head), sharing
 // every K/V tile it loads.  The kernel is persistent: one CTA per SM walks the items.
 // Warp roles (384 threads):
-//   warp 0      TMA producer: the item's Q tiles, then K and V tiles of 128 slots into
-//               two-stage rings (128B-swizzled boxes of 64 dims x 128 slots).
+//   warps 0, 3  TMA producers (warp 0 the item's Q tiles and K, warp 3 V): tiles of 128
+//               slots into two-stage rings (128B-swizzled boxes of 64 dims x 128 slots).
 //   warps 1, 2  MMA issuers, one per query tile (warp 1 also owns TMEM): S = Q K^T
 //               (A, B from shared memory) and O += P V (P from TMEM, V from shared
 //               memory), fp32 accumulators in TMEM.
@@ -426,42 +426,41 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 0 || warp == 3) {
+    // ---------------- TMA producers: warp 0 Q and K, warp 3 V ----------------
+    // (two threads, so that a K load never queues behind a V load waiting for a PV)
     if (lane == 0) {
+      const bool kq = warp == 0;
       int T = 0, n_items_done = 0;           // K/V tiles and items issued so far
       RowCache rc;
-      int k_issued = 0, v_issued = 0, q_issued = 0;
+      int issued = 0, q_issued = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         Item I;
         if (!item_geom(item, pairs, p, meta, rc, &I)) continue;
-        // the previous item's Q tiles are free once its last QK MMA completed
-        if (n_items_done > 0 && !mbar_wait(&sm.q_free, (n_items_done - 1) & 1, abort)) break;
-        mbar_expect_tx(&sm.q_full, 2 * kTileBytes);
-        for (int t = 0; t < 2; ++t)
-          for (int half = 0; half < 2; ++half)
-            tma_load_4d(&tm_q, &sm.q_full, sm.q[t] + half * kBoxBytes, half * 64, I.h, I.row_a + t * kBM, I.b);
-        q_issued = n_items_done + 1;
+        if (kq) {
+          // the previous item's Q tiles are free once its last QK MMA completed
+          if (n_items_done > 0 && !mbar_wait(&sm.q_free, (n_items_done - 1) & 1, abort)) break;
+          mbar_expect_tx(&sm.q_full, 2 * kTileBytes);
+          for (int t = 0; t < 2; ++t)
+            for (int half = 0; half < 2; ++half)
+              tma_load_4d(&tm_q, &sm.q_full, sm.q[t] + half * kBoxBytes, half * 64, I.h, I.row_a + t * kBM, I.b);
+          q_issued = n_items_done + 1;
+        }
+        const CUtensorMap* tm = kq ? &tm_k : &tm_v;
         for (int j = 0; j < I.n_tiles; ++j) {
           const int Tj = T + j, s = Tj % kStages, u = Tj / kStages;
-          const int row = I.row0 + j * kBN;
-          if (Tj >= kStages && !mbar_wait(&sm.k_empty[s], (u - 1) & 1, abort)) {
+          uint64_t* empty = kq ? &sm.k_empty[s] : &sm.v_empty[s];
+          uint64_t* full = kq ? &sm.k_full[s] : &sm.v_full[s];
+          uint8_t* dst = kq ? sm.k[s] : sm.v[s];
+          if (Tj >= kStages && !mbar_wait(empty, (u - 1) & 1, abort)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&sm.k_full[s], kTileBytes);
+          mbar_expect_tx(full, kTileBytes);
           for (int half = 0; half < 2; ++half)
-            tma_load_4d(&tm_k, &sm.k_full[s], sm.k[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
-          k_issued = Tj + 1;
-          if (Tj >= kStages && !mbar_wait(&sm.v_empty[s], (u - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&sm.v_full[s], kTileBytes);
-          for (int half = 0; half < 2; ++half)
-            tma_load_4d(&tm_v, &sm.v_full[s], sm.v[s] + half * kBoxBytes, half * 64, I.kvh, row, I.kv_batch);
-          v_issued = Tj + 1;
+            tma_load_4d(tm, full, dst + half * kBoxBytes, half * 64, I.kvh, I.row0 + j * kBN, I.kv_batch);
+          issued = Tj + 1;
         }
         T += I.n_tiles;
         ++n_items_done;
@@ -469,10 +468,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       if (*abort) {
         // drain: every load this thread issued lands before the CTA's shared memory is released
         if (q_issued > 0) mbar_wait(&sm.q_full, (q_issued - 1) & 1, abort, false);
-        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
-          mbar_wait(&sm.k_full[j % kStages], (j / kStages) & 1, abort, false);
-        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
-          mbar_wait(&sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
+        for (int j = max(0, issued - kStages); j < issued; ++j)
+          mbar_wait(kq ? &sm.k_full[j % kStages] : &sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
       }
     }
   } else if (warp == 1 || warp == 2) {
