@@ -291,10 +291,12 @@ __device__ __forceinline__ float row_max(const uint32_t* sr, int valid) {
 // packed as 16-bit pairs over the first 64 TMEM columns of the row's S; the P of the
 // chunks past kChunks is stored as 0 (the PV MMA reads all 128).  Returns the row sum of
 // p.  Pairs of columns go through the packed fp32x2 FMA / add.
-template <bool kBf16, bool kMask, int kChunks>
-__device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, float c, float m_use, uint32_t s_addr) {
+template <bool kBf16, bool kMask, int kChunks, bool kTrackMax = false>
+__device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, float c, float m_use, uint32_t s_addr,
+                                                float* raw_max = nullptr) {
   const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
   float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   if (kChunks < 4) {
     uint32_t zero[16];
 #pragma unroll
@@ -314,11 +316,20 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, f
         x0 = c0 < valid ? x0 : 0.f;
         x1 = c0 + 1 < valid ? x1 : 0.f;
       }
+      if (kTrackMax) {
+        float s0 = __uint_as_float(sr[c0]), s1 = __uint_as_float(sr[c0 + 1]);
+        if (kMask) {
+          s0 = c0 < valid ? s0 : -INFINITY;
+          s1 = c0 + 1 < valid ? s1 : -INFINITY;
+        }
+        mx[i & 3] = fmax3(mx[i & 3], s0, s1);
+      }
       sum[i & 1] = __fadd2_rn(sum[i & 1], make_float2(x0, x1));
       pk[i] = pack2<kBf16>(x0, x1);
     }
     tmem_st16(s_addr + q4 * 16, pk);
   }
+  if (kTrackMax) *raw_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
   return (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
 }
 
@@ -1001,11 +1012,28 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           tmem_ld_wait();
 #pragma unroll
           for (int q4 = 0; q4 < kC; ++q4) reg_fence32(sr + q4 * 32);
-          const float m_tile = row_max<kM, kC>(sr, valid) * c;
+          // After the first tile, P is computed at once against the current reference
+          // max while the tile's max is found in the same pass; only if that max grew by
+          // more than the threshold (rare) is the tile redone against the new max, so
+          // the result is what the max-first order gives.
+          float m_tile;
+          float lsum = 0.f;
+          if (j > 0) {
+            float raw;
+            lsum = exp_pack_store<kBf16, kM, kC, true>(sr, valid, c, m_ref, s_addr, &raw);
+            m_tile = raw * c;
+          } else {
+            m_tile = row_max<kM, kC>(sr, valid) * c;
+          }
           bool rescale = m_tile > m_ref + kRescaleThreshold;
+          if (j > 0 && !__any_sync(0xffffffffu, rescale)) {
+            l += lsum;
+            return;
+          }
           const float m_new = rescale ? m_tile : m_ref;
           const float m_use = m_new == -INFINITY ? 0.f : m_new;
-          if (__any_sync(0xffffffffu, rescale) && j > 0) {
+          if (j > 0) {
+            tmem_st_wait();                                // the optimistic P is overwritten below
             // O may be rescaled only once PV(T - 1) has finished accumulating into it
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.s_free[(Tj - 1) % kSBufs], ((Tj - 1) / kSBufs) & 1, abort)))
               return;
