@@ -1,7 +1,7 @@
 // Tensor-core chunk attention for bf16 / fp16, D = 128 (sm_103a: tcgen05 + TMEM + TMA).
 // Two kernels share the helpers below: k_attn_tc (a pair of query tiles per item, for
 // stores of at most kShortKv slots per row) and k_attn_1q (one query tile per item with
-// S and O double-buffered in TMEM, for longer stores); the launcher picks by shape.
+// S triple-buffered in TMEM, for longer stores); the launcher picks by shape.
 //
 // Computes, for every query row of a chunk, softmax(scale * q K^T) V over the row's
 // valid slots in physical order: [0, kv_len) of a LINEAR or CIRCULAR store (the
@@ -26,7 +26,8 @@
 //               when the row max grows by more than 2^8; at the end O / l goes to
 //               global memory through 64-byte-swizzled shared staging and TMA stores.
 //               A short last tile (no causal mask) skips its 32-column chunks past the
-//               valid slots.
+//               valid slots; with the causal mask, only a tile that crosses the
+//               diagonal for some row of the warp is masked (a warp vote per tile).
 //   warps 8-11  the same for tile B.
 // TMEM columns: S_A [0,128) S_B [128,256) O_A [256,384) O_B [384,512); P_X occupies the
 // first 64 columns of S_X as packed 16-bit pairs.
@@ -657,17 +658,19 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         using C3 = std::integral_constant<int, 3>;
         using C4 = std::integral_constant<int, 4>;
         using Masked = std::true_type;
-        if (p.causal || valid >= kBN) {   // causal: `valid` differs between rows
-          if (!p.causal) tile(C4{}, std::false_type{});
-          else tile(C4{}, Masked{});
+        // Causal: `valid` differs between rows, and the tile is unmasked only where it covers
+        // every row of this warp; without the mask it is the same for all rows.
+        const bool whole = p.causal ? __all_sync(0xffffffffu, valid >= kBN) : valid >= kBN;
+        if (whole) {
+          tile(C4{}, std::false_type{});
+        } else if (p.causal || valid > 96) {
+          tile(C4{}, Masked{});
         } else if (valid <= 32) {
           tile(C1{}, Masked{});
         } else if (valid <= 64) {
           tile(C2{}, Masked{});
-        } else if (valid <= 96) {
-          tile(C3{}, Masked{});
         } else {
-          tile(C4{}, Masked{});
+          tile(C3{}, Masked{});
         }
         tmem_st_wait();
         tc_fence_before();
@@ -1065,17 +1068,19 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         using C3 = std::integral_constant<int, 3>;
         using C4 = std::integral_constant<int, 4>;
         using Masked = std::true_type;
-        if (p.causal || valid >= kBN) {
-          if (!p.causal) tile(C4{}, std::false_type{});
-          else tile(C4{}, Masked{});
+        // Causal: `valid` differs between rows, and the tile is unmasked only where it covers
+        // every row of this warp; without the mask it is the same for all rows.
+        const bool whole = p.causal ? __all_sync(0xffffffffu, valid >= kBN) : valid >= kBN;
+        if (whole) {
+          tile(C4{}, std::false_type{});
+        } else if (p.causal || valid > 96) {
+          tile(C4{}, Masked{});
         } else if (valid <= 32) {
           tile(C1{}, Masked{});
         } else if (valid <= 64) {
           tile(C2{}, Masked{});
-        } else if (valid <= 96) {
-          tile(C3{}, Masked{});
         } else {
-          tile(C4{}, Masked{});
+          tile(C3{}, Masked{});
         }
         if (*abort) {
           ok = false;

@@ -314,10 +314,14 @@ def test_poisoned_tail_is_never_read(dtype, big, kv_len):
     assert cache.get_error() == 0
 
 
-@pytest.mark.parametrize("n_q,kv_len", [(234, 234), (1, 300), (130, 300), (128, 128), (300, 1000)])
-def test_causal_prefill(n_q, kv_len):
+# capacity 1024: the query-tile-pair kernel; 2048 and 4096: the one-tile kernel.  The
+# longer cases mix whole tiles in range (unmasked path) with the diagonal's masked tiles.
+@pytest.mark.parametrize("n_q,kv_len,cap", [(234, 234, 2048), (1, 300, 2048), (130, 300, 2048), (128, 128, 2048),
+                                            (300, 1000, 2048), (300, 1000, 1024), (700, 1000, 1024),
+                                            (1000, 3000, 4096)])
+def test_causal_prefill(n_q, kv_len, cap):
     H, Hkv, D = 8, 2, 128
-    cache = kvc.KVCache(1, H, Hkv, D, torch.float16, "linear", capacity=2048)
+    cache = kvc.KVCache(1, H, Hkv, D, torch.float16, "linear", capacity=cap)
     g = torch.Generator(device="cuda").manual_seed(n_q * 7 + kv_len)
     cache.k_store.normal_(generator=g)
     cache.v_store.normal_(generator=g)
