@@ -740,7 +740,6 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   if (threadIdx.x == 0 && sm.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 }
 
-// ---- host side ----------------------------------------------------------------
 // ---- one query tile per item: S triple-buffered in TMEM -----------------------------
 // Work item = one 128-row query tile of one (batch row, q head); items run tile-fastest,
 // so the CTAs working at once share a (row, head)'s K/V tiles through L2.  TMEM holds
@@ -1153,6 +1152,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   if (threadIdx.x == 0 && sm.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 }
 
+// ---- host side ----------------------------------------------------------------
 bool make_map(CUtensorMap* m, int dtype, const void* base, uint64_t d1, uint64_t d2, uint64_t d3) {
   return kvc_make_tile_map(m, dtype, base, kD, d1, d2, d3, 128);
 }
@@ -1202,7 +1202,7 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
   // Kernel by shape (a captured graph stays valid at any length): stores whose rows hold
   // at most kShortKv slots (the whole store for PACKED) give items of a few K/V tiles,
   // where the pair kernel's eight softmax warps keep the per-item chain short; longer
-  // stores run the one-tile kernel, whose double-buffered S keeps the tensor pipe fed
+  // stores run the one-tile kernel, whose triple-buffered S keeps the tensor pipe fed
   // (measured crossover between 512 and 1024 slots).
   if (c->cap <= kShortKv) {
     const int64_t items = (int64_t)((n_q + 2 * kBM - 1) / (2 * kBM)) * cfg.heads * cfg.batch;
