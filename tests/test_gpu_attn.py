@@ -334,6 +334,28 @@ def test_causal_prefill(n_q, kv_len, cap):
     assert cache.get_error() == 0
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("cap,lens", [(1024, (1000, 300, 700)), (4096, (1000, 300, 2900))])
+def test_causal_rows_of_different_lengths(dtype, cap, lens):
+    """Each row's queries sit at the end of its own active prefix (query i of n_q at
+    kv_len_b - n_q + i), so the diagonal falls on a different tile and column in every
+    row; bf16 / fp16 run the pair kernel (capacity 1024) or the one-tile kernel (4096),
+    fp32 the SIMT kernel."""
+    H, Hkv, D, n_q = 8, 2, 128, 300
+    cache = kvc.KVCache(len(lens), H, Hkv, D, dtype, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(cap + len(lens))
+    cache.k_store.normal_(generator=g)
+    cache.v_store.normal_(generator=g)
+    cache.set_lengths(kv_len=torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    q = torch.randn(len(lens), n_q, H, D, device="cuda", generator=g).to(dtype)
+    out = cache.attend(q, flags=kvc.CAUSAL)
+    for b, n in enumerate(lens):
+        ref = orc.attend(to64(q[b]), to64(cache.k_store[b, :n]), to64(cache.v_store[b, :n]), causal=True,
+                         q_pos0=n - n_q)
+        assert_close(out[b], ref, f"causal row {b} kv_len {n}")
+    assert cache.get_error() == 0
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
 @pytest.mark.parametrize("cap", [384, 2048])   # short stores: query-tile-pair kernel; long: one-tile kernel
 def test_last_tile_chunk_boundaries(dtype, cap):
