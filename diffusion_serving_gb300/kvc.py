@@ -94,6 +94,8 @@ def _ptr(t):
         return None
     if isinstance(t, int):
         return t
+    if not t.is_contiguous():
+        raise ValueError("kvc: tensors are passed by pointer as dense row-major arrays and must be contiguous")
     return t.data_ptr()
 
 
@@ -228,11 +230,31 @@ class KVCache:
     def advance(self, row=-1, n_tokens=None, stream=None):
         kvc_advance(self.handle, row, self.cfg.chunk if n_tokens is None else n_tokens, stream)
 
+    def _check_rows(self, what, t, heads):
+        """t must be [batch, n, heads, head_dim] in the store's dtype."""
+        shape = (self.cfg.batch, heads, self.cfg.head_dim)
+        if t.dim() != 4 or (t.shape[0], t.shape[2], t.shape[3]) != shape or t.dtype != self.dtype:
+            raise ValueError(f"kvc: {what} must be [{shape[0]}, n, {shape[1]}, {shape[2]}] {self.dtype}, "
+                             f"got {list(t.shape)} {t.dtype}")
+
+    def _check_kv(self, k, v):
+        self._check_rows("k", k, self.cfg.kv_heads)
+        self._check_rows("v", v, self.cfg.kv_heads)
+        if k.shape != v.shape:
+            raise ValueError(f"kvc: k {list(k.shape)} and v {list(v.shape)} differ")
+
+    def _check_q(self, q, out):
+        self._check_rows("q", q, self.cfg.heads)
+        if out.shape != q.shape or out.dtype != q.dtype:
+            raise ValueError(f"kvc: out must match q ({list(q.shape)} {q.dtype})")
+
     def write(self, k, v, slots=None, stream=None):
+        self._check_kv(k, v)
         kvc_write(self.handle, k, v, k.shape[1], slots, stream)
 
     def write_rope(self, k, v, rope, slots=None, stream=None):
         """Write with K rotated by the (cos, sin) table ``rope`` [positions, D/2, 2] fp32."""
+        self._check_kv(k, v)
         kvc_write_rope(self.handle, k, v, k.shape[1], rope, rope.shape[0], slots, stream)
 
     def set_lengths(self, kv_len=None, cu_seqlens=None, stream=None):
@@ -241,6 +263,7 @@ class KVCache:
     def attend(self, q, out=None, flags=0, stream=None):
         if out is None:
             out = torch.empty_like(q)
+        self._check_q(q, out)
         kvc_attend(self.handle, q, out, q.shape[1], flags, stream)
         return out
 
@@ -248,6 +271,7 @@ class KVCache:
         """(out, lse) with lse [B, n_q, H] fp32."""
         if out is None:
             out = torch.empty_like(q)
+        self._check_q(q, out)
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
         kvc_attend_lse(self.handle, q, out, lse, q.shape[1], flags, stream)
         return out, lse

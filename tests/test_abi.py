@@ -81,3 +81,14 @@ def test_null_handle_calls_fail_cleanly():
     assert kvc._lib.kvc_reset(None, -1, None) == kvc.ERR_ARG
     assert kvc._lib.kvc_get_error(None, None, None) == kvc.ERR_ARG
     assert kvc.kvc_strerror(kvc.ERR_RANGE) == "length out of range"
+
+
+def test_binding_rejects_strided_tensors():
+    """The C ABI takes dense row-major arrays: the binding refuses a view with other strides."""
+    import torch
+    with pytest.raises(ValueError):
+        kvc._ptr(torch.empty(4, 8).t())
+    with pytest.raises(ValueError):
+        kvc._ptr(torch.empty(2, 6, 4, 8)[:, ::2])
+    assert kvc._ptr(torch.empty(2, 3, 4, 8)) != 0
+    assert kvc._ptr(None) is None

@@ -150,6 +150,24 @@ def test_host_validation():
         ring.advance(n_tokens=3)
     with pytest.raises(kvc.KvcError):
         ring.write(q[:, :3, :, :], q[:, :3, :, :])
+    # shapes, dtypes and strides the binding refuses before any call
+    lin = kvc.KVCache(2, 4, 2, 64, torch.bfloat16, "linear", capacity=32)
+    lin.advance(n_tokens=8)
+    k = torch.randn(2, 8, 2, 64, device="cuda").bfloat16()
+    for bad_k in (k.half(), k[:, :, :1].contiguous(), torch.randn(2, 8, 4, 64, device="cuda").bfloat16()):
+        with pytest.raises(ValueError):
+            lin.write(bad_k, bad_k)
+    with pytest.raises(ValueError):
+        lin.write(k, k[:, :4].contiguous())
+    qq = torch.randn(2, 5, 4, 64, device="cuda").bfloat16()
+    for bad_q in (qq.half(), qq[:1].contiguous(), torch.randn(2, 5, 2, 64, device="cuda").bfloat16()):
+        with pytest.raises(ValueError):
+            lin.attend(bad_q)
+    with pytest.raises(ValueError):
+        lin.attend(torch.randn(2, 4, 5, 64, device="cuda").bfloat16().transpose(1, 2))
+    with pytest.raises(ValueError):
+        lin.attend(qq, torch.empty(2, 5, 4, 64, device="cuda", dtype=torch.float16))
+    assert lin.get_error() == 0
 
 
 def test_graph_replay_writes_the_device_slot():
