@@ -435,9 +435,7 @@ def ours(args):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "heads": w.heads, "kv_heads": w.kv_heads,
-                   "head_dim": w.head_dim, "chunk": w.chunk, "sink": w.sink, "window": w.window,
-                   "chunks_per_step": w.n_chunks, "rewrites": w.rewrites, "tflop_per_step": step_flops / 1e12,
+        "config": {**workload_config(w),
                    "l2": "inputs larger than L2 (K/V stores %.1f GB)" % (2 * cache.k_store.numel() * 2 / 1e9),
                    "parallelism": f"replicas x{world}"},
         "gpu_launches": launches,
@@ -569,6 +567,13 @@ def ours(args):
         dist.destroy_process_group()
 
 
+def workload_config(w):
+    """The workload's shape, the same in both arms' JSON lines."""
+    return {"workload": w.name, "batch": w.batch, "heads": w.heads, "kv_heads": w.kv_heads,
+            "head_dim": w.head_dim, "chunk": w.chunk, "sink": w.sink, "window": w.window,
+            "chunks_per_step": w.n_chunks, "rewrites": w.rewrites, "tflop_per_step": ring_flops(w)[0] / 1e12}
+
+
 # ---------------------------------------------------------------------------
 # reference arm: the CPU fp64 oracle, timed on the host cores
 # ---------------------------------------------------------------------------
@@ -591,7 +596,8 @@ def reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_total / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
+        "config": {**workload_config(w), "l2": "host memory (fp64 oracle on the host cores)",
+                   "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{rows_total} query rows x {w.window} keys x 1 head per run, fp64 NumPy"},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

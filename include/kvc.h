@@ -28,6 +28,8 @@
  *  - Ownership: the caller owns and allocates every device buffer (K/V store,
  *    meta block, workspace, inputs, outputs).  The library allocates no device
  *    memory; it owns only the host-side handle.  Buffers must outlive the handle.
+ *  - Counts (n_q, n_tokens, n_rows, rope_positions) must be at least 1: an empty
+ *    call is KVC_ERR_ARG, not a no-op, so that a caller's off-by-one surfaces.
  *  - Return value: 0 on success, a negative KVC_ERR_* code otherwise.  Host-side
  *    validation failures enqueue nothing.  Errors found on the device (a slot,
  *    length or offset out of range) never fault: the kernel skips the offending

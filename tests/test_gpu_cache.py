@@ -167,6 +167,16 @@ def test_host_validation():
         lin.attend(torch.randn(2, 4, 5, 64, device="cuda").bfloat16().transpose(1, 2))
     with pytest.raises(ValueError):
         lin.attend(qq, torch.empty(2, 5, 4, 64, device="cuda", dtype=torch.float16))
+    # empty calls are argument errors at the C boundary (kvc.h conventions)
+    out = torch.full_like(qq, 3.0)
+    for call in (lambda: kvc.kvc_attend(lin.handle, qq, out, 0),
+                 lambda: kvc.kvc_write(lin.handle, k, k, 0),
+                 lambda: kvc.kvc_merge(torch.bfloat16, 0, 64, qq, qq, qq, qq, out)):
+        with pytest.raises(kvc.KvcError) as e:
+            call()
+        assert e.value.code == kvc.ERR_ARG
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
     assert lin.get_error() == 0
 
 
