@@ -59,6 +59,11 @@ cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 int launched(cudaError_t e) { return e == cudaSuccess ? KVC_OK : KVC_ERR_CUDA; }
 
+// The write kernels count the K and V source rows of a call (2 x B x n_tokens) in int32.
+bool write_rows_overflow(const kvc_cache* c, int32_t n_tokens) {
+  return 2LL * c->cfg.batch * n_tokens > INT32_MAX;
+}
+
 constexpr uint32_t kFlags = KVC_CAUSAL | KVC_KERNEL_SIMT | KVC_DETERMINISTIC;   // every attend flag
 
 // Kernel choice by shape only: fp32 (or the SIMT flag) -> fp32-FMA kernel; one query
@@ -194,6 +199,7 @@ int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, cons
   if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;
   // a packed write reads a padded source: rows past each row's length are skipped
   if (n_tokens > c->cap && c->cfg.layout != KVC_PACKED) return KVC_ERR_RANGE;
+  if (write_rows_overflow(c, n_tokens)) return KVC_ERR_RANGE;
   if (d_slots != nullptr) {
     if (c->cfg.layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;
     if (((uintptr_t)d_slots & 3u) != 0) return KVC_ERR_ARG;
@@ -208,6 +214,7 @@ int kvc_write_rope(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
   if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;
   if (d_rope == nullptr || ((uintptr_t)d_rope & 7u) != 0 || rope_positions < 1) return KVC_ERR_ARG;
   if (n_tokens > c->cap && c->cfg.layout != KVC_PACKED) return KVC_ERR_RANGE;
+  if (write_rows_overflow(c, n_tokens)) return KVC_ERR_RANGE;
   if (d_slots != nullptr) {
     if (c->cfg.layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;
     if (((uintptr_t)d_slots & 3u) != 0) return KVC_ERR_ARG;

@@ -152,7 +152,8 @@ int kvc_advance(kvc_cache* c, int32_t row, int32_t n_tokens, void* stream);
  *    d_slots[i] — one index shared by all rows on the same timeline [IDX item 1].
  *    Not for PACKED.  Entries outside [0, cap) set KVC_DEV_BAD_SLOT and are skipped.
  * Bytes are copied unchanged (bit-exact).
- * Errors: KVC_ERR_RANGE when n_tokens exceeds the per-row slot count (not PACKED);
+ * Errors: KVC_ERR_RANGE when n_tokens exceeds the per-row slot count (not PACKED) or
+ * 2 x B x n_tokens exceeds INT32_MAX;
  * KVC_ERR_ARG for a circular write whose n_tokens differs from `chunk`. */
 int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
               const int32_t* d_slots, void* stream);
