@@ -22,6 +22,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -88,7 +89,9 @@ class Clocks:
 
     def __init__(self, device_index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples (nvidia-smi CSV); KVC_CLOCKS_DIR keeps them somewhere other than the temp dir
+        self.path = os.path.join(os.environ.get("KVC_CLOCKS_DIR", tempfile.gettempdir()),
+                                 f"kvc_clocks_{os.getpid()}.csv")
         self.dev = device_index
 
     def __enter__(self):
