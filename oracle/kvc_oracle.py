@@ -25,13 +25,23 @@ What it computes, and where each part comes from:
 * Active prefix: attention sees positions ``[0, kv_len)`` (same PR, "Change");
   packed ragged K/V: branch b sees its own ``len_b`` tokens (TensorRT-LLM PR "FA4
   variable-length cross-attention", "Description").
+* ``attend_lse`` adds the log-sum-exp of each row's scaled scores and ``merge_lse``
+  combines two attentions over disjoint key sets from their outputs and LSEs (the
+  forward_with_lse of the same TensorRT-LLM PR); ``rope_apply`` rotates key pairs at
+  their absolute positions (flashdreams issue, "proposed boundary"); ``roll_left`` is
+  the per-step copy a chronological store makes (same issue, "current path").
 
 Parity pins (checked by ``tests/test_oracle.py``): brute-force ring simulation for
 ``ring_slot`` and the attended set; closed forms of attention (one key, equal keys,
 a dominant key, duplicated kv heads); permutation invariance; torch's SDPA in fp64
 on CPU as an independent library routine; the tiny active-prefix fixture printed in
 the fish-speech PR (capacity 8, prefill 3, lengths 3,4,8, bounds 1/8 valid, 0/9
-invalid); packed equal to padded-and-masked.
+invalid); packed equal to padded-and-masked; LSE of one key and of equal keys and
+torch.logsumexp; the merge of two halves equal to attention over their union; RoPE
+against an independent rotation (the input generator's, from its own fp64 angles) and
+its norm and relative-angle invariants; the roll against a deque of chunks.  The pin
+tests also plant mistakes (an off-by-one slot, a wrong attended set, a wrong scale or
+GQA map, a RoPE sign) and check that a pin catches each.
 """
 from __future__ import annotations
 
@@ -230,7 +240,9 @@ class ChronoCache:
 # ---------------------------------------------------------------------------
 def rope_apply(x, positions, table):
     """Rotate pair j = (x[..., 2j], x[..., 2j+1]) of each token by the (cos, sin) that
-    ``table[pos, j]`` holds, in fp64.  x: ``[n, Hkv, D]``; positions: ``[n]``."""
+    ``table[pos, j]`` holds, in fp64.  x: ``[n, Hkv, D]``; positions: ``[n]``.  Keys are
+    rotated at their absolute position before they are stored (flashdreams issue,
+    "proposed boundary")."""
     x = np.asarray(x, dtype=np.float64)
     t = np.asarray(table, dtype=np.float64)[np.asarray(positions)]      # [n, D/2, 2]
     c = t[:, None, :, 0]
@@ -318,7 +330,10 @@ def attend_lse(q, k, v, scale=None, causal=False, q_pos0=0):
 
 def merge_lse(o_a, lse_a, o_b, lse_b):
     """Combine two attentions over disjoint key sets from their outputs and LSEs:
-    o = (e^lse_a o_a + e^lse_b o_b) / (e^lse_a + e^lse_b), lse = log(e^lse_a + e^lse_b)."""
+    o = (e^lse_a o_a + e^lse_b o_b) / (e^lse_a + e^lse_b), lse = log(e^lse_a + e^lse_b).
+    What forward_with_lse outputs are for (TensorRT-LLM PR "FA4 variable-length
+    cross-attention", Microbenchmark paragraph); a side with lse = -inf has no keys and
+    weight 0."""
     o_a, o_b = np.asarray(o_a, np.float64), np.asarray(o_b, np.float64)
     lse_a, lse_b = np.asarray(lse_a, np.float64), np.asarray(lse_b, np.float64)
     lse = np.logaddexp(lse_a, lse_b)
