@@ -1,0 +1,90 @@
+"""Static checks of the CUDA sources (no GPU): every spin-wait is bounded and nothing
+traps.
+
+Each kernel's mbarrier waits go through one helper, ``mbar_wait``, which polls
+``mbarrier.try_wait`` and gives up after a %globaltimer limit (setting the kernel's
+abort flag), so a lost arrival ends the kernel with KVC_DEV_TIMEOUT instead of hanging
+the GPU.  These tests keep it that way: a loop without an exit condition must sit in
+such a helper, ``try_wait`` may be polled nowhere else, and no device code traps or
+asserts.
+"""
+import glob
+import os
+import re
+
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "diffusion_serving_gb300", "csrc")
+SOURCES = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.h")))
+
+
+def code(path):
+    """The source without // and /* */ comments."""
+    text = open(path).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.sub(r"//[^\n]*", "", text)
+
+
+def block_from(text, start):
+    """From `start` to the brace that closes the first `{` after it."""
+    i = text.index("{", start) + 1
+    depth = 1
+    while depth:
+        depth += {"{": 1, "}": -1}.get(text[i], 0)
+        i += 1
+    return text[start:i]
+
+
+def function_bodies(text, name):
+    """Definitions of the bool-returning device helpers called `name`."""
+    return [block_from(text, m.start()) for m in re.finditer(r"\bbool\s+%s\s*\(" % re.escape(name), text)]
+
+
+def test_sources_found():
+    names = {os.path.basename(p) for p in SOURCES}
+    assert {"k_attn_tc.cu", "k_decode.cu", "k_cache.cu", "kvc_api.cu"} <= names
+
+
+def test_unconditional_loops_are_bounded_waits():
+    """A loop without an exit condition is either mbar_wait's polling loop (which has a
+    time limit) or a work loop that leaves with `break` (each of its waits a bounded
+    mbar_wait, checked below); there are no while / do loops to poll a flag with."""
+    for path in SOURCES:
+        text = code(path)
+        name = os.path.basename(path)
+        assert not re.search(r"\bwhile\s*\(", text) and not re.search(r"\bdo\s*\{", text), \
+            f"{name}: a while / do loop (polling loops go through mbar_wait)"
+        bodies = function_bodies(text, "mbar_wait")
+        for m in re.finditer(r"\bfor\s*\([^;)]*;\s*;", text):
+            if any(text.find(b) <= m.start() < text.find(b) + len(b) for b in bodies):
+                continue
+            assert "break;" in block_from(text, m.start()), f"{name}: a loop without an exit condition or break"
+        for b in bodies:
+            assert "globaltimer()" in b and "kTimeoutNs" in b and "return false" in b, \
+                f"{os.path.basename(path)}: mbar_wait without a time limit"
+
+
+def test_try_wait_is_polled_only_by_the_bounded_helper():
+    for path in SOURCES:
+        text = code(path)
+        bodies = function_bodies(text, "mbar_wait")
+        stripped = text
+        for b in bodies:
+            stripped = stripped.replace(b, "")
+        defs = function_bodies(stripped, "mbar_try_wait")
+        for d in defs:
+            stripped = stripped.replace(d, "")
+        assert "mbar_try_wait(" not in stripped, f"{os.path.basename(path)}: try_wait polled outside mbar_wait"
+        assert "mbarrier.try_wait" not in stripped, f"{os.path.basename(path)}: raw try_wait outside the helpers"
+
+
+def test_timeouts_are_short():
+    for path in SOURCES:
+        for m in re.finditer(r"kTimeoutNs\s*=\s*(\d+)ull", code(path)):
+            assert int(m.group(1)) <= 2_000_000_000, f"{os.path.basename(path)}: wait limit above 2 s"
+
+
+def test_no_device_traps_or_asserts():
+    for path in SOURCES:
+        text = code(path)
+        assert "__trap" not in text and not re.search(r"\btrap\s*;", text), os.path.basename(path)
+        assert not re.search(r"(?<!static_)\bassert\s*\(", text), os.path.basename(path)
+        assert "__brkpt" not in text, os.path.basename(path)
