@@ -570,6 +570,73 @@ def ours(args):
         dist.destroy_process_group()
 
 
+def next_rows_bench(kvc, peaks, reps):
+    """The widening rows on the streaming DiT shapes (B2, Hkv 12, D 128, bf16, 4680-token
+    chunks): the write with RoPE fused into K against the plain write of the same chunk
+    (HBM: K and V read and written once, plus the (cos, sin) rows of the chunk's
+    positions), the two-way LSE merge of one chunk's attention outputs (HBM: two partial
+    outputs and LSEs read, one written), and attention with LSE output against plain
+    attention over an 8192-slot store."""
+    w = wl.DIT_STREAM
+    B, H, Hkv, D, C = w.batch, w.heads, w.kv_heads, w.head_dim, w.chunk
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+
+    def time_it(fn):
+        for _ in range(3):
+            fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b) * 1e-3 / reps
+
+    res = {}
+    cache = kvc.KVCache(B, H, Hkv, D, torch.bfloat16, "circular", sink=w.sink, window=w.window, chunk=C)
+    cache.advance()
+    k = torch.randn(B, C, Hkv, D, device="cuda", generator=g).bfloat16()
+    v = torch.randn(B, C, Hkv, D, device="cuda", generator=g).bfloat16()
+    table = wl.rope_table(w.window, D).cuda()
+    t_plain = time_it(lambda: cache.write(k, v))
+    t_rope = time_it(lambda: cache.write_rope(k, v, table))
+    assert cache.get_error() == 0
+    nbytes = 2 * 2 * k.numel() * k.element_size() + C * (D // 2) * 2 * 4
+    res["write_rope"] = {"us": round(t_rope * 1e6, 2), "GB/s": round(nbytes / t_rope / 1e9, 1),
+                         "frac": round(nbytes / t_rope / 1e9 / peaks["hbm"], 4), "bytes": nbytes,
+                         "x_plain_write": round(t_rope / t_plain, 3)}
+    cache.close()
+
+    rows = B * C * H
+    oa = torch.randn(rows, D, device="cuda", generator=g).bfloat16()
+    ob = torch.randn(rows, D, device="cuda", generator=g).bfloat16()
+    la = torch.randn(rows, device="cuda", generator=g)
+    lb = torch.randn(rows, device="cuda", generator=g)
+    out = torch.empty_like(oa)
+    lo = torch.empty_like(la)
+    t_merge = time_it(lambda: kvc.kvc_merge(torch.bfloat16, rows, D, oa, la, ob, lb, out, lo))
+    nbytes = rows * (3 * D * 2 + 3 * 4)
+    res["merge"] = {"rows": rows, "us": round(t_merge * 1e6, 2), "GB/s": round(nbytes / t_merge / 1e9, 1),
+                    "frac": round(nbytes / t_merge / 1e9 / peaks["hbm"], 4), "bytes": nbytes}
+
+    cap = 8192
+    lin = kvc.KVCache(B, H, Hkv, D, torch.bfloat16, "linear", capacity=cap)
+    lin.advance(n_tokens=cap)
+    kk = torch.randn(B, cap, Hkv, D, device="cuda", generator=g).bfloat16()
+    lin.write(kk, kk)
+    q = torch.randn(B, C, H, D, device="cuda", generator=g).bfloat16()
+    o = torch.empty_like(q)
+    lse = torch.empty(B, C, H, dtype=torch.float32, device="cuda")
+    t_att = time_it(lambda: lin.attend(q, o))
+    t_lse = time_it(lambda: kvc.kvc_attend_lse(lin.handle, q, o, lse, C))
+    assert lin.get_error() == 0
+    flops = wl.attention_flops(C, cap, H, D) * B
+    res["attend_lse"] = {"kv_len": cap, "ms": round(t_lse * 1e3, 4), "TFLOP/s": round(flops / t_lse / 1e12, 1),
+                         "x_attend": round(t_lse / t_att, 4)}
+    lin.close()
+    return res
+
+
 def workload_config(w):
     """The workload's shape, the same in both arms' JSON lines."""
     return {"workload": w.name, "batch": w.batch, "heads": w.heads, "kv_heads": w.kv_heads,
@@ -622,7 +689,13 @@ def main():
                     help="time only the ragged cross-attention attends and print them (profiling aid)")
     ap.add_argument("--cross-lq", type=int, default=None,
                     help="padded query count of the cross-attention timing (default: the full workload)")
+    ap.add_argument("--next-rows", action="store_true",
+                    help="time only the RoPE write, the LSE merge and attention with LSE output, and print them")
     args = ap.parse_args()
+    if args.next_rows:
+        from diffusion_serving_gb300 import kvc
+        print(json.dumps({"next_rows": next_rows_bench(kvc, load_peaks(), reps=max(args.steps, 5))}))
+        return
     if args.cross_only:
         from diffusion_serving_gb300 import kvc
         print(json.dumps({"cross_attention": cross_bench(kvc, load_peaks(), reps=args.steps, lq=args.cross_lq)}))
