@@ -1,5 +1,5 @@
-"""Static checks of the CUDA sources (no GPU): every spin-wait is bounded and nothing
-traps.
+"""Static checks of the CUDA sources (no GPU): every spin-wait is bounded, nothing
+traps, and every tiled TMA copy starts on a 16-byte boundary.
 
 Each kernel's mbarrier waits go through one helper, ``mbar_wait``, which polls
 ``mbarrier.try_wait`` and gives up after a %globaltimer limit (setting the kernel's
@@ -88,3 +88,49 @@ def test_no_device_traps_or_asserts():
         assert "__trap" not in text and not re.search(r"\btrap\s*;", text), os.path.basename(path)
         assert not re.search(r"(?<!static_)\bassert\s*\(", text), os.path.basename(path)
         assert "__brkpt" not in text, os.path.basename(path)
+
+
+def call_args(text, start):
+    """Arguments of the call whose '(' follows `start`, split at depth-0 commas."""
+    i = text.index("(", start) + 1
+    depth, cur, args = 1, "", []
+    while True:
+        ch = text[i]
+        if ch in "([{":
+            depth += 1
+        elif ch in ")]}":
+            depth -= 1
+            if depth == 0:
+                args.append(cur.strip())
+                return args
+        if ch == "," and depth == 1:
+            args.append(cur.strip())
+            cur = ""
+        else:
+            cur += ch
+        i += 1
+
+
+def test_tma_inner_coordinate_is_16_byte_aligned():
+    """A tiled cp.async.bulk.tensor copy must start at an innermost coordinate whose byte
+    offset is a multiple of 16: nothing checks it before the copy runs, and a misaligned
+    one stops the context.  Every tensor map is over 16-bit elements (kvc_make_tile_map
+    refuses other types), so x must be a multiple of 8 elements: each call site's x is a
+    multiple of a literal, and that literal a multiple of 8."""
+    api = code(os.path.join(CSRC, "kvc_api.cu"))
+    make = block_from(api, api.index("bool kvc_make_tile_map("))
+    assert "dtype != KVC_BF16 && dtype != KVC_F16" in make and "return false" in make
+    sites = 0
+    for path in SOURCES:
+        text = code(path)
+        for name, x_index in (("tma_load_4d", 3), ("tma_store_4d", 2)):
+            for m in re.finditer(r"\b%s\s*\(" % name, text):
+                if re.search(r"void\s+$", text[max(0, m.start() - 40):m.start()]):
+                    continue                                   # the definition
+                x = call_args(text, m.start())[x_index]
+                lit = re.fullmatch(r"(?:\w+\s*\*\s*(\d+)|(\d+)\s*\*\s*\w+|(\d+))", x)
+                assert lit, f"{os.path.basename(path)}: TMA x coordinate '{x}' is not literal-aligned"
+                assert int(next(g for g in lit.groups() if g)) % 8 == 0, f"{os.path.basename(path)}: x = {x}"
+                sites += 1
+    assert sites >= 8
+
