@@ -1,5 +1,6 @@
 """Static checks of the CUDA sources (no GPU): every spin-wait is bounded, nothing
-traps, and every tiled TMA copy starts on a 16-byte boundary.
+traps, every tiled TMA copy starts on a 16-byte boundary, and the tensor-core MMAs
+never mix operand types.
 
 Each kernel's mbarrier waits go through one helper, ``mbar_wait``, which polls
 ``mbarrier.try_wait`` and gives up after a %globaltimer limit (setting the kernel's
@@ -133,4 +134,20 @@ def test_tma_inner_coordinate_is_16_byte_aligned():
                 assert int(next(g for g in lit.groups() if g)) % 8 == 0, f"{os.path.basename(path)}: x = {x}"
                 sites += 1
     assert sites >= 8
+
+
+def test_mma_operands_share_one_type():
+    """In one tcgen05.mma of kind::f16, A and B must have the same type.  The instruction
+    descriptor takes a single format for both (bits 7-9 for A, 10-12 for B), every
+    descriptor of a kernel is built from the kernel's element type, and P, the A operand
+    of the PV MMA read from TMEM, is packed in that same type."""
+    text = code(os.path.join(CSRC, "k_attn_tc.cu"))
+    body = block_from(text, text.index("constexpr uint32_t idesc_f16("))
+    assert re.search(r"\(fmt << 7\) \| \(fmt << 10\)", body), body
+    calls = re.findall(r"idesc_f16\(([^,]+),", text)
+    calls = [c.strip() for c in calls if not c.strip().startswith("uint32_t")]
+    assert calls and all(c == "kBf16 ? 1u : 0u" for c in calls), calls
+    packs = re.findall(r"pack2<(\w+)>", text)
+    assert packs and all(t == "kBf16" for t in packs), packs
+    assert "kind::f16" in text and "kind::tf32" not in text and "kind::f8f6f4" not in text
 
