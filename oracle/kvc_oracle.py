@@ -28,8 +28,10 @@ What it computes, and where each part comes from:
 * ``attend_lse`` adds the log-sum-exp of each row's scaled scores and ``merge_lse``
   combines two attentions over disjoint key sets from their outputs and LSEs (the
   forward_with_lse of the same TensorRT-LLM PR); ``rope_apply`` rotates key pairs at
-  their absolute positions (flashdreams issue, "proposed boundary"); ``roll_left`` is
-  the per-step copy a chronological store makes (same issue, "current path").
+  their absolute positions (flashdreams issue, "proposed boundary") and ``rope_store``
+  gives what a store of a given type holds after that rotation: the exact rotation
+  rounded once to nearest-even (``round_to_format``); ``roll_left`` is the per-step
+  copy a chronological store makes (same issue, "current path").
 
 Parity pins (checked by ``tests/test_oracle.py``): brute-force ring simulation for
 ``ring_slot`` and the attended set; closed forms of attention (one key, equal keys,
@@ -39,7 +41,10 @@ the fish-speech PR (capacity 8, prefill 3, lengths 3,4,8, bounds 1/8 valid, 0/9
 invalid); packed equal to padded-and-masked; LSE of one key and of equal keys and
 torch.logsumexp; the merge of two halves equal to attention over their union; RoPE
 against an independent rotation (the input generator's, from its own fp64 angles) and
-its norm and relative-angle invariants; the roll against a deque of chunks.  The pin
+its norm and relative-angle invariants; the once-rounded store values against exact
+rational arithmetic (``fractions.Fraction``) on random, tie, near-tie, subnormal and
+overflow cases, and against NumPy's own fp64 -> fp16 / fp32 rounding; the roll against
+a deque of chunks.  The pin
 tests also plant mistakes (an off-by-one slot, a wrong attended set, a wrong scale or
 GQA map, a RoPE sign) and check that a pin catches each.
 """
@@ -251,6 +256,62 @@ def rope_apply(x, positions, table):
     out = np.empty_like(x)
     out[..., 0::2] = x0 * c - x1 * s
     out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
+# Binary formats a store can hold: significand bits p (with the hidden bit), smallest
+# and largest normal exponents.
+FORMATS = {"bf16": (8, -126, 127), "f16": (11, -14, 15), "f32": (24, -126, 127)}
+
+
+def two_sum(a, b):
+    """Knuth's error-free sum in fp64: s = fl(a + b) and the exact rest e, a + b = s + e."""
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    s = a + b
+    bb = s - a
+    e = (a - (s - bb)) + (b - bb)
+    return s, e
+
+
+def round_to_format(hi, lo, fmt):
+    """Round the exact value hi + lo (|lo| at most half an fp64 ulp of hi) to the nearest
+    value of ``fmt``, ties to even, once.  Returns fp64 arrays holding those values (inf
+    past the largest finite value; a zero keeps hi's sign)."""
+    p, emin, emax = FORMATS[fmt]
+    hi = np.asarray(hi, dtype=np.float64)
+    lo = np.asarray(lo, dtype=np.float64)
+    sign = np.where(np.signbit(hi), -1.0, 1.0)
+    a = np.abs(hi)
+    rest = lo * sign                                   # D * sign = a + rest
+    _, e = np.frexp(np.where(a > 0, a, 1.0))           # a = m 2^e, m in [0.5, 1)
+    q = np.maximum(e - 1, emin) - (p - 1)              # exponent of the format's spacing here
+    k = np.ldexp(a, -q)                                # a in units of that spacing (exact)
+    n = np.floor(k)
+    frac_minus_half = (k - n) - 0.5                    # exact
+    d = frac_minus_half + np.ldexp(rest, -q)           # its sign is that of the exact value's
+    up = (d > 0) | ((d == 0) & (np.mod(n, 2) == 1))
+    mag = np.ldexp(n + up, q)
+    largest = np.ldexp(2.0 - 2.0 ** (1 - p), emax)
+    mag = np.where(mag > largest, np.inf, mag)
+    return np.where(a > 0, sign * mag, hi)
+
+
+def rope_store(x, positions, table, fmt):
+    """The rotated keys as a store of format ``fmt`` holds them: the exact rotation of
+    ``rope_apply`` rounded once to ``fmt`` (flashdreams issue, "proposed boundary":
+    keys are rotated at their absolute positions before storage).  x holds values of
+    ``fmt`` and the table fp32 values, so both products are exact in fp64 (at most
+    24 + 24 significant bits); their difference is carried exactly as fp64 plus its
+    rounding error, and rounded to ``fmt`` once.  Returns fp64 values of ``fmt``."""
+    x = np.asarray(x, dtype=np.float64)
+    t = np.asarray(table, dtype=np.float64)[np.asarray(positions)]      # [n, D/2, 2]
+    c = t[:, None, :, 0]
+    s = t[:, None, :, 1]
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = round_to_format(*two_sum(x0 * c, -(x1 * s)), fmt)
+    out[..., 1::2] = round_to_format(*two_sum(x0 * s, x1 * c), fmt)
     return out
 
 

@@ -468,3 +468,120 @@ def test_roll_left_matches_brute_force_deque():
         assert out[b, :S].tolist() == store[b, :S].tolist()
         assert out[b, S:W - C].tolist() == list(rolling)
         assert out[b, W - C:].tolist() == store[b, W - C:].tolist()
+
+
+# ---------------------------------------------------------------------------
+# What a store holds after the fused rotation: the exact rotation rounded once
+# ---------------------------------------------------------------------------
+def round_exact(D, fmt):
+    """Nearest value of ``fmt`` to the rational D, ties to the even significand, by
+    exact rational arithmetic (the textbook definition, independent of fp64)."""
+    from fractions import Fraction as Fr
+    p, emin, emax = orc.FORMATS[fmt]
+    if D == 0:
+        return 0.0
+    sign = -1 if D < 0 else 1
+    a = abs(D)
+    E = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fr(2) ** E > a:
+        E -= 1
+    while Fr(2) ** (E + 1) <= a:
+        E += 1
+    u = Fr(2) ** (max(E, emin) - (p - 1))
+    below = math.floor(a / u)
+    lo_v, hi_v = below * u, (below + 1) * u
+    if a - lo_v < hi_v - a or (a - lo_v == hi_v - a and below % 2 == 0):
+        v = lo_v
+    else:
+        v = hi_v
+    if v > (2 - Fr(2) ** (1 - p)) * Fr(2) ** emax:
+        return sign * math.inf
+    return sign * float(v)
+
+
+def exact_rotation(x0, x1, c, s):
+    from fractions import Fraction as Fr
+    return (Fr(x0) * Fr(c) - Fr(x1) * Fr(s), Fr(x0) * Fr(s) + Fr(x1) * Fr(c))
+
+
+def as_fmt(a, fmt):
+    dt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}[fmt]
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(dt).double().numpy()
+
+
+def rope_cases(fmt, n, seed):
+    """Pairs (x0, x1) of ``fmt`` and fp32 (cos, sin) entries: random magnitudes over
+    many binades, plus constructed ties (the exact product on a midpoint of ``fmt``)
+    and near-ties (a tiny second product pushing it just off), results in the
+    subnormal range and past the largest finite value."""
+    rng = np.random.default_rng(seed)
+    p, emin, emax = orc.FORMATS[fmt]
+    top = {"bf16": 100, "f16": 14, "f32": 100}[fmt]
+    x = as_fmt(rng.standard_normal((n, 2)) * np.exp2(rng.integers(-20, top, (n, 2))), fmt)
+    cs = rng.uniform(-1, 1, (n, 2)).astype(np.float32).astype(np.float64)
+    cs[::7, 1] = np.float32(rng.uniform(-1, 1, len(cs[::7])) * 2.0 ** -30)
+    # ties and near-ties: x0 = 1, cos = a midpoint of fmt (p + 1 significant bits),
+    # x1 * sin = 0, or +-(a 24-bit value) x 2^-60: below half an fp64 ulp of the
+    # midpoint, so the fp64 difference lands on the midpoint and only the exact rest
+    # tells the side
+    k = n // 4
+    mid = (2 ** p + 2 * rng.integers(0, 2 ** (p - 1), k) + 1) / 2.0 ** (p + 1)
+    x[:k, 0] = 1.0
+    cs[:k, 0] = mid
+    x[:k, 1] = as_fmt(np.where(np.arange(k) % 3 == 0, 0.0, 1.0), fmt)
+    tiny = np.float32(rng.uniform(1, 2, k)).astype(np.float64) * 2.0 ** -60
+    cs[:k, 1] = np.where(np.arange(k) % 3 == 1, tiny, -tiny)
+    if fmt == "f16":                       # subnormal results and overflow
+        x[k:k + 8] = [[6.1e-5, 3.0e-5]] * 8
+        x[k + 8:k + 12] = [[65504.0, -65504.0]] * 4
+        cs[k + 8:k + 12] = [[0.75, 0.75]] * 4
+    return x, cs
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16", "f32"])
+def test_rope_store_is_the_exact_rotation_rounded_once(fmt):
+    x, cs = rope_cases(fmt, 1200, {"bf16": 1, "f16": 2, "f32": 3}[fmt])
+    n = len(x)
+    table = cs.reshape(n, 1, 2)                       # one pair per position
+    got = orc.rope_store(x.reshape(n, 1, 2), np.arange(n), table, fmt).reshape(n, 2)
+    from fractions import Fraction as Fr
+    inexact = 0
+    for i in range(n):
+        a, b = exact_rotation(x[i, 0], x[i, 1], cs[i, 0], cs[i, 1])
+        want = (round_exact(a, fmt), round_exact(b, fmt))
+        assert got[i, 0] == want[0] and got[i, 1] == want[1], (i, x[i], cs[i], got[i], want)
+        inexact += Fr(float(a)) != a
+    # the rotation differs from its fp64 rounding in some of these cases (or the pin
+    # would not exercise the carried remainder)
+    assert inexact > 0
+
+
+def test_rope_store_matches_numpy_rounding_where_fp64_is_exact():
+    """With both products of one binade the fp64 rotation is exact, and NumPy's own
+    fp64 -> fp16 / fp32 conversion (correctly rounded) must agree."""
+    from diffusion_serving_gb300 import workloads as wl
+    D = 64
+    table = wl.rope_table(512, D).numpy()
+    x16 = rnd((40, 2, D), 300).astype(np.float16).astype(np.float64)
+    pos = np.arange(3, 43) * 11
+    ref = orc.rope_apply(x16, pos, table)
+    assert np.array_equal(orc.rope_store(x16, pos, table, "f16"),
+                          ref.astype(np.float16).astype(np.float64))
+    x32 = rnd((40, 2, D), 301).astype(np.float32).astype(np.float64)
+    lo_free = orc.rope_store(x32, pos, table, "f32")
+    want = orc.rope_apply(x32, pos, table).astype(np.float32).astype(np.float64)
+    # fp32 inputs: the products have 48 bits, so fp64 rounds some differences; those
+    # may differ from NumPy's conversion only where fp64 landed on an fp32 midpoint
+    assert np.mean(lo_free == want) > 0.999
+
+
+def test_planted_double_rounding_is_caught(monkeypatch):
+    """Rounding the fp64 rotation to the format (two roundings) instead of the exact
+    rotation fails the exact pin on the near-tie cases."""
+    real = orc.round_to_format
+
+    def twice(hi, lo, fmt):
+        return real(hi, np.zeros_like(np.asarray(hi, dtype=np.float64)), fmt)
+    monkeypatch.setattr(orc, "round_to_format", twice)
+    with pytest.raises(AssertionError):
+        test_rope_store_is_the_exact_rotation_rounded_once("bf16")
