@@ -1,5 +1,8 @@
-"""Comparison helpers shared by the GPU parity tests (no method arithmetic)."""
+"""Comparison helpers shared by the GPU parity tests: tolerances and error bounds, no
+method arithmetic beyond what a bound needs."""
 from __future__ import annotations
+
+import math
 
 import numpy as np
 import torch
@@ -58,3 +61,58 @@ def assert_close(got_t: torch.Tensor, ref: np.ndarray, what: str = ""):
     bad, ties = argmax_check(got, ref, dtype)
     assert bad == 0, f"{what}: {bad} row argmax mismatches ({ties} near-tie rows)"
     return float(err.max()), float(err.mean())
+
+
+# Error bound of a log-sum-exp computed by the attention kernels (natural log units).
+# Each kernel forms scores with fp32 accumulation, exponentiates s * scale * log2(e) - m
+# with an approximate exp2, sums the terms in fp32 with a running-max rescale, and
+# returns (m + log2 l) * ln 2.  Bounding each step, for a row with fp64 scores s_j,
+# softmax weights w_j and n keys:
+#  * dot products: each of the D additions of an fp32 accumulation (any order, rounded
+#    or truncated) errs by at most one fp32 ulp (2^-23) of a partial sum no larger than
+#    sum_d |q_d k_jd|; allowing 2D such steps covers blocked accumulation, so score j
+#    errs by B_j = scale * 2D * 2^-23 * sum_d |q_d k_jd|.  The LSE moves by at most the
+#    w-weighted mean of the score errors (mean-value theorem; the factor e^(2 max B)
+#    covers the weights moving with the scores).
+#  * exponent arguments: rounding s * (scale log2 e) and the subtraction of the
+#    running max, 2^-23 |s_j| + ln2 2^-24 |t_j| (t_j the argument of exp2), weighted by w.
+#  * exponentials: relative error eps_e = 2^-21 per term and per rescale factor (above
+#    the relative error PTX states for ex2.approx.f32 and CUDA states for exp2f), with at
+#    most T = ceil(n/16) + 160 rescales of the running sum (one per 16-slot tile, plus
+#    split and warp merges).
+#  * fp32 sums: every term passes through at most A = ceil(n/4) + 64 additions (the
+#    longest per-thread chain, the decode kernel's), 2^-24 each.
+#  * the final log2, add and multiply by ln 2: 2^-21 (|LSE| + 1).
+# A relative error x of the sum moves the log by at most x / (1 - x).
+EPS_EXP2 = 2.0 ** -21
+
+
+def lse_error_bound(q, k, scale, lse_ref):
+    """Per-row bound [n_q, H] on |LSE_gpu - LSE_exact| for fp64 q [n_q, H, D], the keys
+    k [n, Hkv, D] one row attends and the oracle's LSE [n_q, H] (rows with keys)."""
+    n_q, H, D = q.shape
+    n, Hkv, _ = k.shape
+    G = H // Hkv
+    T = -(-n // 16) + 160
+    A = -(-n // 4) + 64
+    rel_sum = (2 + T) * EPS_EXP2 + A * 2.0 ** -24
+    out = np.empty((n_q, H))
+    for h in range(H):
+        kh = k[:, h // G, :]
+        s = scale * (q[:, h, :] @ kh.T)                          # [n_q, n]
+        w = np.exp(s - lse_ref[:, h][:, None])
+        B = scale * 2 * D * 2.0 ** -23 * (np.abs(q[:, h, :]) @ np.abs(kh).T)
+        t = (s - s.max(axis=1, keepdims=True)) / math.log(2)
+        dots = np.exp(2 * B.max(axis=1)) * (w * B).sum(axis=1)
+        args = (w * (2.0 ** -23 * np.abs(s) + math.log(2) * 2.0 ** -24 * np.abs(t))).sum(axis=1)
+        out[:, h] = dots + args + rel_sum / (1 - rel_sum) + 2.0 ** -21 * (np.abs(lse_ref[:, h]) + 1)
+    return out
+
+
+def merge_lse_error_bound(lse_a, lse_b, bound_a, bound_b):
+    """Bound on the merged LSE: the merge is 1-Lipschitz in its two inputs (max of their
+    bounds), plus its own fp32 arithmetic (expf within 2 ulp, logf within 1 ulp, the
+    rounding of the difference of the inputs and of the final add)."""
+    L = np.logaddexp(lse_a, lse_b)
+    own = 2.0 ** -20 + 2.0 ** -23 * (np.abs(L) + np.abs(lse_a - lse_b))
+    return np.maximum(bound_a, bound_b) + own

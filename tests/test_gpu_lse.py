@@ -10,14 +10,21 @@ import pytest
 import torch
 
 from oracle import kvc_oracle as orc
-from tests.helpers import assert_close, to64
+from tests.helpers import assert_close, lse_error_bound, merge_lse_error_bound, to64
 
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
     from diffusion_serving_gb300 import kvc
 
-LSE_ATOL = 2e-3
+
+
+def check_lse(got, q, k, ref_l, what=""):
+    """Every row's LSE within the bound derived from the kernels' arithmetic."""
+    bound = lse_error_bound(q, k, orc.default_scale(q.shape[-1]), ref_l)
+    err = np.abs(got - ref_l)
+    assert np.all(err <= bound), f"{what}: LSE error {err.max():.3e} above its bound at {np.argmax(err - bound)}"
+    return bound
 
 
 def filled_linear(B, H, Hkv, D, dtype, cap, lens, seed):
@@ -46,7 +53,7 @@ def test_attend_lse_matches_oracle(dtype, n_q, flags, H, Hkv):
     for b in range(B):
         ref_o, ref_l = orc.attend_lse(to64(q[b]), to64(c.k_store[b, :lens[b]]), to64(c.v_store[b, :lens[b]]))
         assert_close(out[b], ref_o, f"row {b}")
-        assert np.abs(lse[b].cpu().double().numpy() - ref_l).max() < LSE_ATOL
+        check_lse(lse[b].cpu().double().numpy(), to64(q[b]), to64(c.k_store[b, :lens[b]]), ref_l, f"row {b}")
     assert c.get_error() == 0
 
 
@@ -77,11 +84,17 @@ def test_split_then_merge_equals_whole(dtype):
     kvc.kvc_merge(dtype, rows, D, o_a, l_a, o_b, l_b, merged, l_m)
     torch.cuda.synchronize()
     ref_o, ref_l = orc.attend_lse(to64(q[0]), to64(k[0]), to64(v[0]))
+    _, ref_a = orc.attend_lse(to64(q[0]), to64(k[0, :n_a]), to64(v[0, :n_a]))
+    _, ref_b = orc.attend_lse(to64(q[0]), to64(k[0, n_a:]), to64(v[0, n_a:]))
     assert_close(merged[0], ref_o, "merged vs oracle")
-    assert np.abs(l_m[0].cpu().double().numpy() - ref_l).max() < LSE_ATOL
+    b_a = check_lse(l_a[0].cpu().double().numpy(), to64(q[0]), to64(k[0, :n_a]), ref_a, "half a")
+    b_b = check_lse(l_b[0].cpu().double().numpy(), to64(q[0]), to64(k[0, n_a:]), ref_b, "half b")
+    b_w = check_lse(l_w[0].cpu().double().numpy(), to64(q[0]), to64(k[0]), ref_l, "whole")
+    b_m = merge_lse_error_bound(ref_a, ref_b, b_a, b_b)
+    assert np.all(np.abs(l_m[0].cpu().double().numpy() - ref_l) <= b_m), "merged LSE above its bound"
     # the merged result agrees with the one-store attention within rounding of the halves
     assert (merged.float() - o_w.float()).abs().max().item() < 1e-2
-    assert (l_m - l_w).abs().max().item() < LSE_ATOL
+    assert np.all(np.abs((l_m - l_w)[0].cpu().double().numpy()) <= b_m + b_w)
 
 
 def test_merge_rows_without_keys():
@@ -100,4 +113,9 @@ def test_merge_rows_without_keys():
     assert torch.all(out[:4] == 0) and torch.all(torch.isneginf(lo[:4]))
     assert np.abs(to64(out) - ref_o).max() < 1e-2
     fin = np.isfinite(ref_l)
-    assert np.abs(lo.double().cpu().numpy()[fin] - ref_l[fin]).max() < 1e-5
+    la64, lb64 = la.double().cpu().numpy(), lb.double().cpu().numpy()
+    zero = np.zeros(rows)
+    with np.errstate(invalid="ignore"):
+        bound = merge_lse_error_bound(la64, lb64, zero, zero)
+    bound = np.where(np.isfinite(la64) & np.isfinite(lb64), bound, 2.0 ** -20 + 2.0 ** -23 * np.abs(ref_l))
+    assert np.all(np.abs(lo.double().cpu().numpy()[fin] - ref_l[fin]) <= bound[fin])
