@@ -69,6 +69,12 @@ def _load():
         "kvc_destroy": (ctypes.c_int, [P]),
         "kvc_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvc_attend_decode_noalloc": (ctypes.c_int, [cfgp, P, P, P, P, P, P]),
+        "kvc_lengths_bytes": (SZ, [I32]),
+        "kvc_lengths_create": (ctypes.c_int, [I32, I32, I32, P, P, ctypes.POINTER(P)]),
+        "kvc_lengths_set": (ctypes.c_int, [P, P, P, P]),
+        "kvc_use_lengths": (ctypes.c_int, [P, P]),
+        "kvc_lengths_destroy": (ctypes.c_int, [P]),
+        "kvc_debug_stall_waits": (ctypes.c_int, [P, ctypes.c_uint64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -197,15 +203,88 @@ def kvc_strerror(code: int) -> str:
     return _lib.kvc_strerror(code).decode()
 
 
+def _check_noalloc_args(cfg: kvc_config, k_store, v_store, meta, q, out):
+    """The C call reads and writes through these pointers with sizes taken from cfg, so a
+    tensor smaller than cfg says, or of another type, is refused here."""
+    dt = CODE_DTYPE.get(cfg.dtype)
+    want = (cfg.batch, 1, cfg.heads, cfg.head_dim)
+    for name, t in (("q", q), ("out", out)):
+        if tuple(t.shape) != want or t.dtype != dt:
+            raise ValueError(f"kvc: {name} must be {list(want)} {dt}, got {list(t.shape)} {t.dtype}")
+    rows = {LINEAR: cfg.batch * cfg.capacity, CIRCULAR: cfg.batch * cfg.window, PACKED: cfg.capacity}.get(cfg.layout, 0)
+    need = rows * cfg.kv_heads * cfg.head_dim
+    for name, t in (("k_store", k_store), ("v_store", v_store)):
+        if t.dtype != dt or t.numel() < need:
+            raise ValueError(f"kvc: {name} must hold {need} {dt} elements, got {t.numel()} {t.dtype}")
+    mb = kvc_meta_bytes(cfg)
+    if meta.dtype != torch.int32 or meta.numel() * 4 < mb:
+        raise ValueError(f"kvc: meta must be int32 of at least {mb} bytes, got {meta.numel()} {meta.dtype}")
+
+
 def kvc_attend_decode_noalloc(cfg: kvc_config, k_store, v_store, meta, q, out, stream=None) -> None:
     """Decode attention for callers that cannot allocate device memory (see kvc.h)."""
+    _check_noalloc_args(cfg, k_store, v_store, meta, q, out)
     _check(_lib.kvc_attend_decode_noalloc(ctypes.byref(cfg), _ptr(k_store), _ptr(v_store), _ptr(meta), _ptr(q),
                                           _ptr(out), _stream(stream)), "kvc_attend_decode_noalloc")
 
 
+def kvc_debug_stall_waits(h: int, ns: int) -> None:
+    """Testing hook: the handle's later attends wait ns nanoseconds on a barrier nothing
+    signals, then give up (KVC_DEV_TIMEOUT); 0 turns it off."""
+    _check(_lib.kvc_debug_stall_waits(h, ns), "kvc_debug_stall_waits")
+
+
+def kvc_lengths_bytes(batch: int) -> int:
+    return _lib.kvc_lengths_bytes(batch)
+
+
+def kvc_lengths_create(batch: int, layout, capacity: int, block, stream=None) -> int:
+    lay = LAYOUT_CODE[layout] if isinstance(layout, str) else int(layout)
+    h = ctypes.c_void_p()
+    _check(_lib.kvc_lengths_create(batch, lay, capacity, _ptr(block), _stream(stream), ctypes.byref(h)),
+           "kvc_lengths_create")
+    return h.value
+
+
+def kvc_lengths_set(L: int, kv_len=None, cu_seqlens=None, stream=None) -> None:
+    _check(_lib.kvc_lengths_set(L, _ptr(kv_len), _ptr(cu_seqlens), _stream(stream)), "kvc_lengths_set")
+
+
+def kvc_use_lengths(h: int, L) -> None:
+    _check(_lib.kvc_use_lengths(h, L), "kvc_use_lengths")
+
+
+def kvc_lengths_destroy(L: int) -> None:
+    _check(_lib.kvc_lengths_destroy(L), "kvc_lengths_destroy")
+
+
 # ---------------------------------------------------------------------------
-# convenience owner of the device buffers
+# convenience owners of the device buffers
 # ---------------------------------------------------------------------------
+class KVLengths:
+    """A shared length layout (kv_len per row, or packed cu_seqlens) over a torch-allocated
+    block; handles point at it with ``KVCache.use_lengths``."""
+
+    def __init__(self, batch, layout, capacity, device="cuda", stream=None):
+        self.batch = batch
+        nbytes = kvc_lengths_bytes(batch)
+        self.block = torch.zeros(nbytes // 4, dtype=torch.int32, device=device)
+        self.handle = kvc_lengths_create(batch, layout, capacity, self.block, stream)
+
+    def set(self, kv_len=None, cu_seqlens=None, stream=None):
+        kvc_lengths_set(self.handle, kv_len, cu_seqlens, stream)
+
+    def close(self):
+        if self.handle:
+            kvc_lengths_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
 class KVCache:
     """A kvc handle plus torch-allocated K/V stores, meta block and workspace."""
 
@@ -259,6 +338,12 @@ class KVCache:
 
     def set_lengths(self, kv_len=None, cu_seqlens=None, stream=None):
         kvc_set_lengths(self.handle, kv_len, cu_seqlens, stream)
+
+    def use_lengths(self, lengths: "KVLengths | None"):
+        """Read lengths from a shared layout (None: from this handle's own meta block).
+        The layout object is kept referenced so that it outlives this use."""
+        kvc_use_lengths(self.handle, None if lengths is None else lengths.handle)
+        self.shared_lengths = lengths
 
     def attend(self, q, out=None, flags=0, stream=None):
         if out is None:

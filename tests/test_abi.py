@@ -11,7 +11,7 @@ from diffusion_serving_gb300 import kvc
 
 def test_library_exports_every_declared_function():
     names = kvc.header_functions()
-    assert len(names) == 17
+    assert len(names) == 23
     for n in names:
         assert hasattr(kvc._lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", kvc.LIB_PATH], capture_output=True, text=True).stdout
@@ -92,3 +92,42 @@ def test_binding_rejects_strided_tensors():
         kvc._ptr(torch.empty(2, 6, 4, 8)[:, ::2])
     assert kvc._ptr(torch.empty(2, 3, 4, 8)) != 0
     assert kvc._ptr(None) is None
+
+
+def test_binding_refuses_mismatched_noalloc_buffers():
+    """kvc_attend_decode_noalloc takes only pointers; its wrapper checks the tensors
+    against the config before any call, so a wrong q / out shape or type, an undersized
+    store or meta block never reaches the library (no device is needed for this)."""
+    import torch
+    c = kvc.make_config(2, 8, 2, 64, torch.float16, "linear", capacity=32)
+    store = torch.zeros(2 * 32 * 2 * 64, dtype=torch.float16)
+    meta = torch.zeros(kvc.kvc_meta_bytes(c) // 4, dtype=torch.int32)
+    q = torch.zeros(2, 1, 8, 64, dtype=torch.float16)
+    bad = {
+        "q shape": dict(q=torch.zeros(2, 2, 8, 64, dtype=torch.float16)),
+        "q dtype": dict(q=torch.zeros(2, 1, 8, 64, dtype=torch.bfloat16)),
+        "out shape": dict(out=torch.zeros(2, 1, 4, 64, dtype=torch.float16)),
+        "store size": dict(k_store=store[:-1]),
+        "store dtype": dict(v_store=torch.zeros(2 * 32 * 2 * 64, dtype=torch.float32)),
+        "meta size": dict(meta=meta[:-1]),
+        "meta dtype": dict(meta=torch.zeros(64, dtype=torch.float32)),
+    }
+    for what, change in bad.items():
+        args = dict(k_store=store, v_store=store, meta=meta, q=q, out=q.clone())
+        args.update(change)
+        with pytest.raises(ValueError):
+            kvc._check_noalloc_args(c, **args)
+    kvc._check_noalloc_args(c, store, store, meta, q, q.clone())      # the matching set passes
+
+
+def test_shared_lengths_host_checks():
+    """Length layouts: sizes and the host-side refusals, before any device work."""
+    assert kvc.kvc_lengths_bytes(0) == 0
+    assert kvc.kvc_lengths_bytes(2) == kvc.kvc_meta_bytes(cfg(batch=2, layout="packed", capacity=64))
+    h = ctypes.c_void_p()
+    assert kvc._lib.kvc_lengths_create(2, kvc.CIRCULAR, 64, 256, None, ctypes.byref(h)) == kvc.ERR_UNSUPPORTED
+    assert kvc._lib.kvc_lengths_create(0, kvc.PACKED, 64, 256, None, ctypes.byref(h)) == kvc.ERR_ARG
+    assert kvc._lib.kvc_lengths_create(2, kvc.PACKED, 64, 8, None, ctypes.byref(h)) == kvc.ERR_ARG   # misaligned
+    assert kvc._lib.kvc_lengths_create(2, kvc.PACKED, 64, None, None, ctypes.byref(h)) == kvc.ERR_ARG
+    assert kvc._lib.kvc_lengths_set(None, 16, None, None) == kvc.ERR_ARG
+    assert kvc._lib.kvc_use_lengths(None, None) == kvc.ERR_ARG
