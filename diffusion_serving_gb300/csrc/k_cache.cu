@@ -105,8 +105,8 @@ constexpr int kWriteUnroll = 4;
 
 __global__ void __launch_bounds__(kWriteThreads)
 k_write(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* __restrict__ kdst,
-        uint4* __restrict__ vdst, int32_t* __restrict__ meta, const int32_t* __restrict__ slots, int B, int n,
-        int row_vecs, int cap, int layout) {
+        uint4* __restrict__ vdst, int32_t* __restrict__ meta, const int32_t* __restrict__ lens,
+        const int32_t* __restrict__ slots, int B, int n, int row_vecs, int cap, int layout) {
   kvc_pdl_wait();
   kvc_pdl_release();
   const int lane = threadIdx.x & 31;
@@ -120,7 +120,7 @@ k_write(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* _
     const int i = e - b * n;
     int64_t drow = -1;
     if (layout == KVC_PACKED) {
-      const int32_t* cu = meta + kvc_meta_cu(B);
+      const int32_t* cu = lens + kvc_meta_cu(B);
       const int lo = cu[b], hi = cu[b + 1];
       if (i < hi - lo && lo >= 0 && hi <= cap) drow = lo + i;
     } else if (slots != nullptr) {
@@ -159,80 +159,162 @@ k_write(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* _
 // circular KV policy for streaming attention", "proposed boundary": absolute positions
 // determine RoPE before storage).  Pair j of a head, (x[2j], x[2j+1]), turns by the
 // angle whose (cos, sin) the caller's table holds at [pos][j]:
-//   (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos), fp32 FMAs for 16-bit stores (fp64 for
-//   fp32 stores), rounded once to the store type.
+//   (x0, x1) -> (x0 cos - x1 sin, x0 sin + x1 cos),
+// and the store receives the exact value of each component rounded once to nearest-even
+// in the store type (finite inputs).
 // Absolute position of token i: CIRCULAR (chunks - 1) * chunk + i; LINEAR base + i, or
 // slots[i] when slots are given; PACKED i.  Rows whose position is outside the table
 // are skipped and set KVC_DEV_BAD_POS.
+//
+// Rounding once, 16-bit stores.  Component a*b - c*d (a, c of the store type, exact in
+// fp32; b, d fp32 table entries; the second component x0 sin + x1 cos is x0*sin -
+// x1*(-cos)).  Fast path, in fp32 (two components per packed fp32x2 instruction):
+//   q = c*d, its error eq = fma(c, d, -q) (exact while |c*d| >= 2^-100, or zero when c or
+//   d is), r = fma(a, b, -q), r2 = r - eq.
+// Then |r2 - (a*b - c*d)| <= half an ulp of r2 plus half an ulp of r; with
+// |q| <= 2^20 |r2| (no deep cancellation) r is within a binade of r2, so the error is at
+// most 1.5 ulp of r2.  Rounding r2 gives the answer unless r2 lies within 2 fp32 ulps of a
+// rounding midpoint of the store type, which its low bits show (16 of them for bf16, 13
+// for fp16 normal values).  Every other element (a fraction of a percent with N(0, 1)
+// data, plus fp16 subnormal results) takes the exact path: in fp64 the products are exact
+// (<= 35 significant bits), hi = fl(a*b - c*d) with its exact rest (Knuth's TwoSum), and
+// hi + rest is rounded to fp32 by round-to-odd (truncate, then set the last bit when
+// inexact), which has enough spare bits for one correct rounding to the store type.
+__device__ __forceinline__ void kvc_two_sum(double a, double b, double& s, double& e) {
+  s = a + b;
+  const double bb = s - a;
+  e = (a - (s - bb)) + (b - bb);
+}
+
+// a*b - c*d rounded to fp32 by round-to-odd.
+__device__ __noinline__ float kvc_rot_odd(float a, float b, float c, float d) {
+  double hi, rest;
+  kvc_two_sum((double)a * (double)b, -((double)c * (double)d), hi, rest);
+  const float t = __double2float_rz(hi);
+  uint32_t u = __float_as_uint(t);
+  if ((double)t == hi) {
+    if (rest == 0.0) return t;                       // exact
+    if ((rest > 0.0) != (hi > 0.0)) u -= 1;          // the exact value is just inside t
+  }
+  return __uint_as_float(u | 1u);
+}
+
+template <typename T> struct Round16;
+template <> struct Round16<__nv_bfloat16> {
+  using T2 = __nv_bfloat162;
+  __device__ static float2 unpack(T2 h) { return __bfloat1622float2(h); }
+  __device__ static T2 pack(float a, float b) { return __floats2bfloat162_rn(a, b); }
+  __device__ static __nv_bfloat16 rn(float x) { return __float2bfloat16_rn(x); }
+  // r2 is more than 2 fp32 ulps away from every bf16 rounding midpoint
+  __device__ static bool clear(float r2) { return (__float_as_uint(r2) & 0xFFFFu) - 0x7FFEu > 4u; }
+};
+template <> struct Round16<__half> {
+  using T2 = __half2;
+  __device__ static float2 unpack(T2 h) { return __half22float2(h); }
+  __device__ static T2 pack(float a, float b) { return __floats2half2_rn(a, b); }
+  __device__ static __half rn(float x) { return __float2half_rn(x); }
+  __device__ static bool clear(float r2) {
+    const float m = fabsf(r2);
+    if (m >= 65536.f) return true;                   // every such value rounds to infinity
+    return m >= 0x1p-14f && (__float_as_uint(r2) & 0x1FFFu) - 0x0FFEu > 4u;
+  }
+};
+
+// Per-lane constants of one pair: (cos, sin), (sin, -cos), (-sin, cos).
+struct RopePair {
+  float2 cs, sc, nsc;
+};
+
 template <typename T> struct Pack;
-template <> struct Pack<__nv_bfloat16> {
+template <typename T> struct Pack16 {
+  using R = Round16<T>;
   static constexpr int kPairs = 4;   // pairs per 16-byte vector
-  __device__ static void rot(uint4& u, const float2* cs) {
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+  __device__ static void rot(uint4& u, const RopePair* cp) {
+    typename R::T2* h = reinterpret_cast<typename R::T2*>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float2 x = __bfloat1622float2(h[i]);
-      const float2 c = cs[i];
-      h[i] = __floats2bfloat162_rn(fmaf(x.x, c.x, -x.y * c.y), fmaf(x.x, c.y, x.y * c.x));
+      const float2 x = R::unpack(h[i]);
+      const float2 x1 = make_float2(x.y, x.y);
+      const float2 nq = __fmul2_rn(x1, cp[i].nsc);                          // -q
+      const float2 eq = __ffma2_rn(x1, cp[i].sc, nq);                       // exact error of q
+      const float2 r = __ffma2_rn(make_float2(x.x, x.x), cp[i].cs, nq);
+      const float2 r2 = __ffma2_rn(eq, make_float2(-1.f, -1.f), r);         // r - eq
+      const float qa = fabsf(nq.x), qb = fabsf(nq.y);
+      const bool ok_a = ((qa >= 0x1p-100f && qa <= fabsf(r2.x) * 0x1p20f) ||
+                         (qa == 0.f && (x.y == 0.f || cp[i].sc.x == 0.f))) && R::clear(r2.x);
+      const bool ok_b = ((qb >= 0x1p-100f && qb <= fabsf(r2.y) * 0x1p20f) ||
+                         (qb == 0.f && (x.y == 0.f || cp[i].sc.y == 0.f))) && R::clear(r2.y);
+      if (ok_a && ok_b) {
+        h[i] = R::pack(r2.x, r2.y);
+      } else {
+        const float a = ok_a ? r2.x : kvc_rot_odd(x.x, cp[i].cs.x, x.y, cp[i].sc.x);
+        const float b = ok_b ? r2.y : kvc_rot_odd(x.x, cp[i].cs.y, x.y, cp[i].sc.y);
+        h[i] = R::pack(a, b);   // r2 itself where it was clear, the odd-rounded value elsewhere
+      }
     }
   }
 };
-template <> struct Pack<__half> {
-  static constexpr int kPairs = 4;
-  __device__ static void rot(uint4& u, const float2* cs) {
-    __half2* h = reinterpret_cast<__half2*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x = __half22float2(h[i]);
-      const float2 c = cs[i];
-      h[i] = __floats2half2_rn(fmaf(x.x, c.x, -x.y * c.y), fmaf(x.x, c.y, x.y * c.x));
-    }
-  }
-};
-// fp32 stores turn the pair in fp64 and round once, so that the stored value is the
-// correctly rounded rotation (fp32 arithmetic would leave ~1 ulp of its own rounding).
+template <> struct Pack<__nv_bfloat16> : Pack16<__nv_bfloat16> {};
+template <> struct Pack<__half> : Pack16<__half> {};
+// fp32 stores: the products (<= 48 significant bits) are exact in fp64; hi = fl(a*b - c*d)
+// with its exact rest (TwoSum).  Rounding hi to fp32 is the answer unless hi sits exactly
+// on an fp32 midpoint with a non-zero rest, in which case the rest's sign picks the side.
+__device__ __forceinline__ float kvc_rot_round_f32(float a, float b, float c, float d) {
+  double hi, rest;
+  kvc_two_sum((double)a * (double)b, -((double)c * (double)d), hi, rest);
+  const float f = __double2float_rn(hi);
+  if (rest == 0.0) return f;
+  const float lo_f = __double2float_rd(hi), hi_f = __double2float_ru(hi);
+  if (lo_f == hi_f) return f;
+  const double up = isinf(hi_f) ? copysign(0x1p128, (double)hi_f) : (double)hi_f;
+  const double down = isinf(lo_f) ? copysign(0x1p128, (double)lo_f) : (double)lo_f;
+  if (hi != 0.5 * (up + down)) return f;
+  return rest > 0.0 ? hi_f : lo_f;
+}
 template <> struct Pack<float> {
   static constexpr int kPairs = 2;
-  __device__ static void rot(uint4& u, const float2* cs) {
+  __device__ static void rot(uint4& u, const RopePair* cp) {
     float* f = reinterpret_cast<float*>(&u);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const double x0 = f[2 * i], x1 = f[2 * i + 1];
-      const double c = cs[i].x, sn = cs[i].y;
-      f[2 * i] = (float)fma(x0, c, -x1 * sn);
-      f[2 * i + 1] = (float)fma(x0, sn, x1 * c);
+      const float x0 = f[2 * i], x1 = f[2 * i + 1];
+      f[2 * i] = kvc_rot_round_f32(x0, cp[i].cs.x, x1, cp[i].sc.x);
+      f[2 * i + 1] = kvc_rot_round_f32(x0, cp[i].cs.y, x1, cp[i].sc.y);
     }
   }
 };
 
+// One warp per token (b, i): it resolves the destination row and the position once, then
+// its lanes load the token's K and V vectors together (V is stored as it came, K after
+// the rotation), so the copy of V keeps memory busy while K is rotated.
 template <typename T>
 __global__ void __launch_bounds__(kWriteThreads)
 k_write_rope(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* __restrict__ kdst,
-             uint4* __restrict__ vdst, int32_t* __restrict__ meta, const int32_t* __restrict__ slots,
-             const float2* __restrict__ rope, int rope_positions, int B, int n, int row_vecs, int cap, int layout,
-             int chunk, int head_dim) {
+             uint4* __restrict__ vdst, int32_t* __restrict__ meta, const int32_t* __restrict__ lens,
+             const int32_t* __restrict__ slots, const float2* __restrict__ rope, int rope_positions, int B, int n,
+             int row_vecs, int cap, int layout, int chunk, int head_dim) {
   constexpr int P = Pack<T>::kPairs;
+  constexpr int U = 3;                    // vectors of K (and of V) in flight per lane
+  kvc_pdl_wait();
+  kvc_pdl_release();
   const int lane = threadIdx.x & 31;
-  const int rows_per_tensor = B * n;
-  const int rows = 2 * rows_per_tensor;
+  const int tokens = B * n;
   const int warps = (gridDim.x * blockDim.x) >> 5;
   const int half_d = head_dim / 2;
-  for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
-    const int t = r >= rows_per_tensor;
-    const int e = r - (t ? rows_per_tensor : 0);
+  for (int e = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; e < tokens; e += warps) {
     const int b = e / n;
     const int i = e - b * n;
     int64_t drow = -1;
     int pos = -1;
     if (layout == KVC_PACKED) {
-      const int32_t* cu = meta + kvc_meta_cu(B);
+      const int32_t* cu = lens + kvc_meta_cu(B);
       const int lo = cu[b], hi = cu[b + 1];
       if (i < hi - lo && lo >= 0 && hi <= cap) drow = lo + i;
       pos = i;
     } else if (slots != nullptr) {
       const int sl = slots[i];
       if (sl >= 0 && sl < cap) drow = (int64_t)b * cap + sl;
-      else if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_SLOT);
+      else if (lane == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_SLOT);
       pos = sl;
     } else {
       const int32_t* m = meta + kvc_meta_row(b);
@@ -240,27 +322,51 @@ k_write_rope(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uin
       const int sl = m[KVC_ROW_BASE] + i;
       const bool ok = chunks > 0 && sl >= 0 && sl < cap && (layout != KVC_LINEAR || sl < m[KVC_ROW_FILLED]);
       if (ok) drow = (int64_t)b * cap + sl;
-      else if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, chunks > 0 ? KVC_DEV_BAD_SLOT : KVC_DEV_NO_CHUNK);
+      else if (lane == 0) atomicOr(meta + KVC_META_ERR, chunks > 0 ? KVC_DEV_BAD_SLOT : KVC_DEV_NO_CHUNK);
       pos = layout == KVC_CIRCULAR ? (chunks - 1) * chunk + i : sl;
     }
     if (drow < 0) continue;
     if (pos < 0 || pos >= rope_positions) {        // neither K nor V of such a token is written
-      if (lane == 0 && t == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_POS);
+      if (lane == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_BAD_POS);
       continue;
     }
-    const uint4* src = (t ? vsrc : ksrc) + (int64_t)e * row_vecs;
-    uint4* dst = (t ? vdst : kdst) + drow * row_vecs;
-    const float2* cs_row = rope + (int64_t)pos * half_d;
-    for (int v = lane; v < row_vecs; v += 32) {
-      uint4 val = __ldg(src + v);
-      if (t == 0) {
-        const int pair0 = (v * P) % half_d;        // first pair of this vector within its head
-        float2 cs[P];
+    // A lane's vectors v, v + 32, ... all start at the same pair of their head: 32
+    // vectors of P pairs span whole heads (head_dim / 2 is 32 or 64 pairs), so the
+    // lane's (cos, sin) entries are read once per token.
+    RopePair cp[P];
+    {
+      const float2* cs_row = rope + (int64_t)pos * half_d + (lane * P) % half_d;
 #pragma unroll
-        for (int k = 0; k < P; ++k) cs[k] = __ldg(cs_row + pair0 + k);
-        Pack<T>::rot(val, cs);
+      for (int k = 0; k < P; ++k) {
+        const float2 t = __ldg(cs_row + k);
+        cp[k].cs = t;
+        cp[k].sc = make_float2(t.y, -t.x);
+        cp[k].nsc = make_float2(-t.y, t.x);
       }
-      dst[v] = val;
+    }
+    const uint4* ks = ksrc + (int64_t)e * row_vecs;
+    const uint4* vs = vsrc + (int64_t)e * row_vecs;
+    uint4* kd = kdst + drow * row_vecs;
+    uint4* vd = vdst + drow * row_vecs;
+    for (int v0 = lane; v0 < row_vecs; v0 += 32 * U) {
+      uint4 kv[U], vv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (v0 + 32 * u < row_vecs) {
+          kv[u] = __ldg(ks + v0 + 32 * u);
+          vv[u] = __ldg(vs + v0 + 32 * u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (v0 + 32 * u < row_vecs) vd[v0 + 32 * u] = vv[u];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (v0 + 32 * u < row_vecs) {
+          Pack<T>::rot(kv[u], cp);
+          kd[v0 + 32 * u] = kv[u];
+        }
+      }
     }
   }
 }
@@ -313,6 +419,11 @@ cudaError_t kvc_launch_set_lengths(kvc_cache* c, const int32_t* kv_len, const in
   return kvc_launch_pdl(k_set_lengths, dim3(1), dim3(128), 0, s, c->meta, c->cfg.batch, c->cap, kv_len, cu);
 }
 
+cudaError_t kvc_launch_set_lengths_block(int32_t* block, int B, int cap, const int32_t* kv_len, const int32_t* cu,
+                                         cudaStream_t s) {
+  return kvc_launch_pdl(k_set_lengths, dim3(1), dim3(128), 0, s, block, B, cap, kv_len, cu);
+}
+
 cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
                              cudaStream_t s) {
   const kvc_config& g = c->cfg;
@@ -323,27 +434,27 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
   return kvc_launch_pdl(k_write, dim3((unsigned)blocks), dim3(kWriteThreads), 0, s, (const uint4*)k, (const uint4*)v,
-                        (uint4*)c->k, (uint4*)c->v, c->meta, slots, g.batch, n, row_vecs, c->cap, g.layout);
+                        (uint4*)c->k, (uint4*)c->v, c->meta, c->lens, slots, g.batch, n, row_vecs, c->cap,
+                        g.layout);
 }
 
 cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
                                   const float* rope, int rope_positions, cudaStream_t s) {
   const kvc_config& g = c->cfg;
   const int row_vecs = g.kv_heads * g.head_dim * c->eb / 16;
-  const int64_t rows = 2LL * g.batch * n;
-  int64_t blocks = (rows + kWriteThreads / 32 - 1) / (kWriteThreads / 32);
+  const int64_t tokens = (int64_t)g.batch * n;
+  int64_t blocks = (tokens + kWriteThreads / 32 - 1) / (kWriteThreads / 32);
   const int64_t max_blocks = (int64_t)c->num_sms * 8;
   if (blocks > max_blocks) blocks = max_blocks;
   if (blocks < 1) blocks = 1;
 #define KVC_WR(T)                                                                                               \
-  k_write_rope<T><<<(unsigned)blocks, kWriteThreads, 0, s>>>(                                                   \
-      (const uint4*)k, (const uint4*)v, (uint4*)c->k, (uint4*)c->v, c->meta, slots, (const float2*)rope,         \
-      rope_positions, g.batch, n, row_vecs, c->cap, g.layout, g.chunk, g.head_dim)
-  if (g.dtype == KVC_F32) KVC_WR(float);
-  else if (g.dtype == KVC_F16) KVC_WR(__half);
-  else KVC_WR(__nv_bfloat16);
+  kvc_launch_pdl(k_write_rope<T>, dim3((unsigned)blocks), dim3(kWriteThreads), 0, s, (const uint4*)k,          \
+                 (const uint4*)v, (uint4*)c->k, (uint4*)c->v, c->meta, c->lens, slots, (const float2*)rope,     \
+                 rope_positions, g.batch, n, row_vecs, c->cap, g.layout, g.chunk, g.head_dim)
+  if (g.dtype == KVC_F32) return KVC_WR(float);
+  if (g.dtype == KVC_F16) return KVC_WR(__half);
+  return KVC_WR(__nv_bfloat16);
 #undef KVC_WR
-  return cudaGetLastError();
 }
 
 cudaError_t kvc_launch_roll(kvc_cache* c, void* scratch, cudaStream_t s) {
