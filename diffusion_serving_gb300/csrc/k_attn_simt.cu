@@ -53,7 +53,7 @@ k_attn_simt(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ 
   const int kvh = h / (g.H / g.Hkv);
 
   int row0 = 0, len = 0;
-  if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;  // uniform per block
+  if (!kvc_row_range(g, b, &row0, &len, meta + KVC_META_ERR)) return;  // uniform per block
 
   // stage this block's query rows (pre-scaled into the exp2 domain)
   for (int e = threadIdx.x; e < kRowsPerBlock * D; e += blockDim.x) {
@@ -150,7 +150,7 @@ k_attn_simt(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ 
 template <typename T>
 cudaError_t launch_t(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse, cudaStream_t s) {
   const kvc_config& cfg = c->cfg;
-  kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
+  kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout, c->lens};
   dim3 grid((n_q + kRowsPerBlock - 1) / kRowsPerBlock, cfg.heads, cfg.batch);
   const float sl2 = c->scale * 1.4426950408889634f;
   if (cfg.head_dim == 64)

@@ -64,6 +64,15 @@ constexpr uint32_t kStageBytes = 32 * 32 * 2;        // 32 rows x 32 dims, 16-bi
 constexpr uint64_t kTimeoutNs = 500000000ull;   // 0.5 s; a healthy wait is microseconds
 constexpr float kRescaleThreshold = 8.0f;            // log2 units
 
+// Per-CTA abort flag and the limit of its steady-state waits (kTimeoutNs, or the testing
+// hook's stall_ns); waits while draining after an abort always use kTimeoutNs.
+struct WaitCtl {
+  int abort;
+  int stall;           // testing hook: steady-state waits wait on `never` instead
+  uint64_t limit_ns;
+  uint64_t never;      // an mbarrier nothing arrives on
+};
+
 struct Smem {
   // 1024-byte aligned tiles (128B swizzle atoms)
   uint8_t q[2][kTileBytes];
@@ -80,7 +89,7 @@ struct Smem {
   uint64_t s_full[2], p_ready[2], o_done[2];
   uint64_t drain[2];
   uint32_t tmem_base;
-  int abort;
+  WaitCtl wc;
 };
 
 static_assert(sizeof(Smem) + 1024 <= 232448, "shared memory above the 227 KB a block may opt into");
@@ -122,15 +131,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Bounded wait for the phase with the given parity.  Returns false when the CTA is
 // aborting (another role gave up) or when this wait ran out of time (then it starts
 // the abort itself).  `honour_abort` = false is used while draining.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, bool honour_abort = true) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile WaitCtl* w,
+                                          bool honour_abort = true) {
+  if (honour_abort && w->stall) {   // the failure-path test: a wait that nothing ends
+    bar = const_cast<uint64_t*>(&w->never);
+    parity = 0;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = honour_abort ? (uint64_t)w->limit_ns : (uint64_t)kTimeoutNs;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 63) == 0) {
-      if (honour_abort && *abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
-        *abort = 1;
+      if (honour_abort && w->abort) return false;
+      if (globaltimer() - t0 > limit) {
+        w->abort = 1;
         return false;
       }
     }
@@ -340,6 +355,8 @@ struct TcParams {
   int causal;
   float scale_log2;
   float* lse;        // optional [B, n_q, H] natural-log log-sum-exp of each row's scaled scores
+  uint64_t stall_ns; // testing hook: > 0 makes steady-state waits wait this long on a barrier
+                     // nothing arrives on (then the CTA aborts); 0 in normal use
 };
 
 // Work item = one pair of 128-row query tiles (A, B) of one (batch row, q head), in the
@@ -366,7 +383,7 @@ __device__ __forceinline__ bool item_geom(int item, int pairs, const TcParams& p
   it->row_a = pair * 2 * kBM;
   if (it->b != rc.b) {
     rc.b = it->b;
-    rc.ok = kvc_row_range(meta, g, it->b, &rc.row0, &rc.len, meta + KVC_META_ERR);
+    rc.ok = kvc_row_range(g, it->b, &rc.row0, &rc.len, meta + KVC_META_ERR);
   }
   if (!rc.ok) return false;
   const int len = rc.len;
@@ -402,11 +419,14 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 
   // a CTA that starts after another one gave up on a wait returns at once (one read,
   // shared, so that every thread takes the same branch)
-  if (threadIdx.x == 0)
-    sm.abort = (*reinterpret_cast<volatile int32_t*>(meta + KVC_META_ERR) & KVC_DEV_TIMEOUT) ? 1 : 0;
+  if (threadIdx.x == 0) {
+    sm.wc.abort = (*reinterpret_cast<volatile int32_t*>(meta + KVC_META_ERR) & KVC_DEV_TIMEOUT) ? 1 : 0;
+    sm.wc.limit_ns = p.stall_ns > 0 ? p.stall_ns : kTimeoutNs;
+    sm.wc.stall = p.stall_ns > 0;
+  }
   __syncthreads();
-  if (sm.abort) return;
-  volatile int* abort = &sm.abort;
+  if (sm.wc.abort) return;
+  volatile WaitCtl* abort = &sm.wc;
 
   if (threadIdx.x == 0) {
     mbar_init(&sm.q_full, 1);
@@ -427,6 +447,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     mbar_init(&sm.tok[1], 1);
     mbar_init(&sm.drain[0], 1);
     mbar_init(&sm.drain[1], 1);
+    mbar_init(&sm.wc.never, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -477,7 +498,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         T += I.n_tiles;
         ++n_items_done;
       }
-      if (*abort) {
+      if (abort->abort) {
         // drain: every load this thread issued lands before the CTA's shared memory is released
         if (q_issued > 0) mbar_wait(&sm.q_full, (q_issued - 1) & 1, abort, false);
         for (int j = max(0, issued - kStages); j < issued; ++j)
@@ -582,7 +603,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       T += I.n_tiles;
       ++n_items_done;
     }
-    if (*abort && lane == 0) {
+    if (abort->abort && lane == 0) {
       // drain: all MMAs issued by this thread complete before TMEM is released
       mma_commit(&sm.drain[t]);
       mbar_wait(&sm.drain[t], 0, abort, false);
@@ -737,7 +758,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && sm.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
+  if (threadIdx.x == 0 && sm.wc.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 }
 
 // ---- one query tile per item: S triple-buffered in TMEM -----------------------------
@@ -768,7 +789,7 @@ struct Smem1 {
   uint64_t o_done, o_free;
   uint64_t drain[2];
   uint32_t tmem_base;
-  int abort;
+  WaitCtl wc;
 };
 static_assert(sizeof(Smem1) + 1024 <= 232448, "shared memory above the 227 KB a block may opt into");
 static_assert(offsetof(Smem1, o_stage) % 1024 == 0, "staging buffers must keep the swizzle phase of their address");
@@ -783,7 +804,7 @@ __device__ __forceinline__ bool item_geom1(int item, int qtiles, const TcParams&
   it->row_a = qt * kBM;
   if (it->b != rc.b) {
     rc.b = it->b;
-    rc.ok = kvc_row_range(meta, g, it->b, &rc.row0, &rc.len, meta + KVC_META_ERR);
+    rc.ok = kvc_row_range(g, it->b, &rc.row0, &rc.len, meta + KVC_META_ERR);
   }
   if (!rc.ok) return false;
   const int len = rc.len;
@@ -811,11 +832,14 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   const int qtiles = (p.n_q + kBM - 1) / kBM;
   const int n_items = g.B * g.H * qtiles;
 
-  if (threadIdx.x == 0)
-    sm.abort = (*reinterpret_cast<volatile int32_t*>(meta + KVC_META_ERR) & KVC_DEV_TIMEOUT) ? 1 : 0;
+  if (threadIdx.x == 0) {
+    sm.wc.abort = (*reinterpret_cast<volatile int32_t*>(meta + KVC_META_ERR) & KVC_DEV_TIMEOUT) ? 1 : 0;
+    sm.wc.limit_ns = p.stall_ns > 0 ? p.stall_ns : kTimeoutNs;
+    sm.wc.stall = p.stall_ns > 0;
+  }
   __syncthreads();
-  if (sm.abort) return;
-  volatile int* abort = &sm.abort;
+  if (sm.wc.abort) return;
+  volatile WaitCtl* abort = &sm.wc;
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -836,6 +860,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
+    mbar_init(&sm.wc.never, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -885,7 +910,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         T += I.n_tiles;
         ++n;
       }
-      if (*abort) {
+      if (abort->abort) {
         // drain: every load this thread issued lands before the CTA's shared memory is released
         for (int m = max(0, q_issued - 2); m < q_issued; ++m) mbar_wait(&sm.q_full[m & 1], (m >> 1) & 1, abort, false);
         for (int j = max(0, issued - kStages); j < issued; ++j)
@@ -926,7 +951,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       T += I.n_tiles;
       ++n;
     }
-    if (*abort && lane == 0) {
+    if (abort->abort && lane == 0) {
       mma_commit(&sm.drain[0]);
       mbar_wait(&sm.drain[0], 0, abort, false);
     }
@@ -975,7 +1000,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       T += I.n_tiles;
       ++n;
     }
-    if (*abort && lane == 0) {
+    if (abort->abort && lane == 0) {
       mma_commit(&sm.drain[1]);
       mbar_wait(&sm.drain[1], 0, abort, false);
     }
@@ -1081,7 +1106,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         } else {
           tile(C3{}, Masked{});
         }
-        if (*abort) {
+        if (abort->abort) {
           ok = false;
           break;
         }
@@ -1149,7 +1174,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  if (threadIdx.x == 0 && sm.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
+  if (threadIdx.x == 0 && sm.wc.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 }
 
 // ---- host side ----------------------------------------------------------------
@@ -1194,11 +1219,12 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
   if (!kvc_make_tile_map(&tm_o, cfg.dtype, out, kD, cfg.heads, (uint64_t)n_q, cfg.batch, 32, KVC_BOX_SW64))
     return cudaErrorInvalidValue;
   TcParams p;
-  p.g = kvc_geom{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
+  p.g = kvc_geom{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout, c->lens};
   p.n_q = n_q;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = c->scale * 1.4426950408889634f;
   p.lse = lse;
+  p.stall_ns = c->debug_stall_ns;
   // Kernel by shape (a captured graph stays valid at any length): stores whose rows hold
   // at most kShortKv slots (the whole store for PACKED) give items of a few K/V tiles,
   // where the pair kernel's eight softmax warps keep the per-item chain short; longer

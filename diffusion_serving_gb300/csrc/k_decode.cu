@@ -68,17 +68,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait (0.5 s of %globaltimer); false when it ran out or the block is aborting.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+// Per-block abort flag and the limit of its steady-state waits (kTimeoutNs, or the
+// testing hook's stall_ns); waits while draining after an abort always use kTimeoutNs.
+struct WaitCtl {
+  int abort;
+  int stall;           // testing hook: steady-state waits wait on `never` instead
+  uint64_t limit_ns;
+  uint64_t never;      // an mbarrier nothing arrives on
+};
+
+// Bounded wait; false when it ran out or the block is aborting.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile WaitCtl* w,
                                           bool honour_abort = true) {
+  if (honour_abort && w->stall) {   // the failure-path test: a wait that nothing ends
+    bar = const_cast<uint64_t*>(&w->never);
+    parity = 0;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
+  const uint64_t limit = honour_abort ? (uint64_t)w->limit_ns : (uint64_t)kTimeoutNs;
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 63) == 0) {
-      if (honour_abort && *abort) return false;
-      if (globaltimer() - t0 > kTimeoutNs) {
-        *abort = 1;
+      if (honour_abort && w->abort) return false;
+      if (globaltimer() - t0 > limit) {
+        w->abort = 1;
         return false;
       }
     }
@@ -155,7 +169,7 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
 k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const T* __restrict__ q,
          T* __restrict__ out, int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2,
-         float* __restrict__ lse, int fixed_tiles) {
+         float* __restrict__ lse, int fixed_tiles, uint64_t stall_ns) {
   constexpr int HB = D / 64;         // 64-dim boxes per K (or V) tile
   constexpr int NT = D / 8;          // n-tiles of 8 dims in O
   constexpr uint32_t SB = stage_bytes<D>();
@@ -166,7 +180,8 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   float (*s_acc)[G][D] = reinterpret_cast<float (*)[G][D]>(dsm);
   __shared__ float s_ml[kWarps][G][2];
   __shared__ float s_inv[G], s_max[G];
-  __shared__ int s_last, s_abort;
+  __shared__ int s_last;
+  __shared__ WaitCtl s_wc;
   __shared__ int s_tile[kStages];    // tile index held by each stage, -1: no more tiles
 
   const int split = blockIdx.x, nsplit = gridDim.x;
@@ -178,7 +193,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   kvc_pdl_wait();
   kvc_pdl_release();
   int row0 = 0, len = 0;
-  if (!kvc_row_range(meta, g, b, &row0, &len, meta + KVC_META_ERR)) return;
+  if (!kvc_row_range(g, b, &row0, &len, meta + KVC_META_ERR)) return;
 
   // Tiles of kTile slots of this row: block `split` takes tiles split, split + nsplit, ...
   // for its first kStages tiles, then claims tiles kStages * nsplit, ... one at a time
@@ -200,10 +215,15 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     mbar_init(&full[threadIdx.x], 1);
     mbar_init(&empty[threadIdx.x], kWarps);
   }
-  if (threadIdx.x == 0) s_abort = 0;
+  if (threadIdx.x == 0) {
+    s_wc.abort = 0;
+    s_wc.stall = stall_ns > 0;
+    s_wc.limit_ns = stall_ns > 0 ? stall_ns : kTimeoutNs;
+    mbar_init(&s_wc.never, 1);
+  }
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   __syncthreads();
-  volatile int* abort = &s_abort;
+  volatile WaitCtl* abort = &s_wc;
 
   if (warp == kWarps) {
     // ---------------- producer: TMA tiles of K and V into the stage ring ----------------
@@ -244,7 +264,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         if (!step(t + 1, cb)) break;
         cb = claim_for(t + 3);
       }
-      if (*abort) {   // let every load issued here land before the block releases its shared memory
+      if (abort->abort) {   // let every load issued here land before the block releases its shared memory
         for (int t = max(0, issued - kStages); t < issued; ++t)
           mbar_wait(&full[t % kStages], (t / kStages) & 1, abort, false);
       }
@@ -366,7 +386,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     }
   }
   __syncthreads();
-  if (threadIdx.x == 0 && s_abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
+  if (threadIdx.x == 0 && s_wc.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
 
   // ---- this block's partial: merge the warps ---------------------------------
   if (solo) {   // the whole row: normalise and write the output
@@ -500,10 +520,11 @@ cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, int fi
   constexpr size_t smem = dyn_smem_bytes<D>();
   if (prepare) return cudaFuncSetAttribute(k_decode<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const kvc_config& cfg = c->cfg;
-  kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout};
+  kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout, c->lens};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
   return kvc_launch_pdl(k_decode<T, D, G>, grid, dim3(kThreads), smem, s, c->tm_dk, c->tm_dv, (const T*)q, (T*)out,
-                        c->meta, (float*)c->ws, g, c->scale * 1.4426950408889634f, lse, fixed);
+                        c->meta, (float*)c->ws, g, c->scale * 1.4426950408889634f, lse, fixed,
+                        c->debug_stall_ns);
 }
 
 template <typename T, int D>
@@ -646,6 +667,7 @@ extern "C" int kvc_attend_decode_noalloc(const kvc_config* cfg, const void* k_st
   c.k = const_cast<void*>(k_store);
   c.v = const_cast<void*>(v_store);
   c.meta = meta;
+  c.lens = meta;
   c.ws = scratch;
   c.dec_splits = splits;
   if (!kvc_make_decode_maps(&c)) return KVC_ERR_CUDA;

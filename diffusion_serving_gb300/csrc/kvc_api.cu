@@ -157,6 +157,8 @@ int kvc_create(const kvc_config* cfg, void* k_store, void* v_store, void* meta, 
   c->k = k_store;
   c->v = v_store;
   c->meta = reinterpret_cast<int32_t*>(meta);
+  c->lens = c->meta;
+  c->bound = nullptr;
   c->ws = workspace;
   c->dec_splits = kvc_decode_supported(*cfg) ? decode_splits(*cfg, cap) : 0;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
@@ -231,6 +233,59 @@ int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_s
   return launched(kvc_launch_set_lengths(c, d_kv_len, d_cu_seqlens, as_stream(stream)));
 }
 
+size_t kvc_lengths_bytes(int32_t batch) {
+  if (batch < 1) return 0;
+  const size_t words = (size_t)kvc_meta_cu(batch) + batch + 1;
+  return (words * 4 + 255) & ~(size_t)255;
+}
+
+int kvc_lengths_create(int32_t batch, int32_t layout, int32_t capacity, void* d_block, void* stream,
+                       kvc_lengths** out) {
+  if (out == nullptr) return KVC_ERR_ARG;
+  *out = nullptr;
+  if (batch < 1 || capacity < 1 || d_block == nullptr || !aligned16(d_block)) return KVC_ERR_ARG;
+  if (layout != KVC_LINEAR && layout != KVC_PACKED) return KVC_ERR_UNSUPPORTED;
+  kvc_lengths* L = new (std::nothrow) kvc_lengths();
+  if (L == nullptr) return KVC_ERR_ARG;
+  L->batch = batch;
+  L->layout = layout;
+  L->cap = capacity;
+  L->block = reinterpret_cast<int32_t*>(d_block);
+  if (cudaMemsetAsync(d_block, 0, kvc_lengths_bytes(batch), as_stream(stream)) != cudaSuccess) {
+    delete L;
+    return KVC_ERR_CUDA;
+  }
+  *out = L;
+  return KVC_OK;
+}
+
+int kvc_lengths_set(kvc_lengths* L, const int32_t* d_kv_len, const int32_t* d_cu_seqlens, void* stream) {
+  if (L == nullptr || (d_kv_len == nullptr && d_cu_seqlens == nullptr)) return KVC_ERR_ARG;
+  if (d_kv_len != nullptr && L->layout == KVC_PACKED) return KVC_ERR_UNSUPPORTED;
+  if (d_cu_seqlens != nullptr && L->layout != KVC_PACKED) return KVC_ERR_UNSUPPORTED;
+  return launched(kvc_launch_set_lengths_block(L->block, L->batch, L->cap, d_kv_len, d_cu_seqlens,
+                                               as_stream(stream)));
+}
+
+int kvc_use_lengths(kvc_cache* c, const kvc_lengths* L) {
+  if (c == nullptr) return KVC_ERR_ARG;
+  if (L == nullptr) {
+    c->lens = c->meta;
+    c->bound = nullptr;
+    return KVC_OK;
+  }
+  if (L->batch != c->cfg.batch || L->cap > c->cap) return KVC_ERR_ARG;
+  if (L->layout != c->cfg.layout) return KVC_ERR_UNSUPPORTED;
+  c->lens = L->block;
+  c->bound = L;
+  return KVC_OK;
+}
+
+int kvc_lengths_destroy(kvc_lengths* L) {
+  delete L;
+  return KVC_OK;
+}
+
 int kvc_attend(kvc_cache* c, const void* q, void* out, int32_t n_q, uint32_t flags, void* stream) {
   if (c == nullptr || !q || !out || !aligned16(q) || !aligned16(out) || n_q < 1) return KVC_ERR_ARG;
   if (flags & ~kFlags) return KVC_ERR_ARG;
@@ -276,10 +331,15 @@ int kvc_reset(kvc_cache* c, int32_t row, void* stream) {
 int kvc_get_error(kvc_cache* c, void* stream, int32_t* bits) {
   if (c == nullptr) return KVC_ERR_ARG;
   cudaStream_t s = as_stream(stream);
-  int32_t word = 0;
+  int32_t word = 0, shared = 0;
+  int32_t* shared_word = c->bound != nullptr ? c->bound->block + KVC_META_ERR : nullptr;
   if (cudaMemcpyAsync(&word, c->meta + KVC_META_ERR, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      (shared_word != nullptr &&
+       cudaMemcpyAsync(&shared, shared_word, sizeof(shared), cudaMemcpyDeviceToHost, s) != cudaSuccess) ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return KVC_ERR_CUDA;
+  if (shared != 0 && cudaMemsetAsync(shared_word, 0, sizeof(int32_t), s) != cudaSuccess) return KVC_ERR_CUDA;
+  word |= shared;
   if (bits != nullptr) *bits = word;
   if (word == 0) return KVC_OK;
   if (cudaMemsetAsync(c->meta + KVC_META_ERR, 0, sizeof(int32_t), s) != cudaSuccess) return KVC_ERR_CUDA;
@@ -293,6 +353,12 @@ int kvc_get_error(kvc_cache* c, void* stream, int32_t* bits) {
   }
   if (cudaStreamSynchronize(s) != cudaSuccess) return KVC_ERR_CUDA;
   return KVC_ERR_DEVICE;
+}
+
+int kvc_debug_stall_waits(kvc_cache* c, uint64_t ns) {
+  if (c == nullptr) return KVC_ERR_ARG;
+  c->debug_stall_ns = ns;
+  return KVC_OK;
 }
 
 int kvc_destroy(kvc_cache* c) {

@@ -17,6 +17,15 @@
 __host__ __device__ inline int kvc_meta_row(int b) { return KVC_META_ROW0 + 4 * b; }
 __host__ __device__ inline int kvc_meta_cu(int B) { return KVC_META_ROW0 + 4 * B; }
 
+// A length layout shared by several handles: a caller-owned device block in the meta
+// block's layout (error word, per-row kv_len, cu_seqlens) for `batch` rows.
+struct kvc_lengths {
+  int batch;
+  int layout;     // KVC_LINEAR (kv_len) or KVC_PACKED (cu_seqlens)
+  int cap;        // the largest length (LINEAR) or packed total it accepts
+  int32_t* block;
+};
+
 struct kvc_cache {
   kvc_config cfg;
   int cap;            // slots per row (LINEAR capacity, CIRCULAR window) or packed total
@@ -25,10 +34,14 @@ struct kvc_cache {
   void* k;
   void* v;
   int32_t* meta;
+  const int32_t* lens;       // where attends and packed writes read kv_len / cu_seqlens:
+                             // meta, or the block of a shared length layout (kvc_use_lengths)
+  const kvc_lengths* bound;  // that shared layout, or null
   void* ws;
   int device;
   int num_sms;
   int dec_splits;     // split-KV decode: splits per (row, kv head); 0 = no decode kernel
+  uint64_t debug_stall_ns;   // testing hook (kvc_debug_stall_waits); 0 in normal use
   bool tc_ok;         // the tensor-core chunk kernel serves this config
   CUtensorMap tm_k;   // K store, 128B-swizzled boxes of 64 dims x 128 slots (tensor-core kernel)
   CUtensorMap tm_v;   // V store, same boxes
@@ -42,12 +55,13 @@ struct kvc_cache {
 // row0_b = cu_seqlens[b].
 struct kvc_geom {
   int B, H, Hkv, D, cap, layout;
+  const int32_t* lens;   // lengths block in the meta layout (the handle's meta or a shared layout)
 };
 
-// Valid slot range of row b read from the meta block on the device.  Returns false
-// (and sets the error word) when the row's length is out of range.
-__device__ __forceinline__ bool kvc_row_range(const int32_t* meta, const kvc_geom& g, int b,
-                                              int* row0, int* len, int32_t* err_word) {
+// Valid slot range of row b, read on the device from the lengths block g.lens.
+// Returns false (and sets the error word) when the row's length is out of range.
+__device__ __forceinline__ bool kvc_row_range(const kvc_geom& g, int b, int* row0, int* len, int32_t* err_word) {
+  const int32_t* meta = g.lens;
   if (g.layout == KVC_PACKED) {
     const int32_t* cu = meta + kvc_meta_cu(g.B);
     int lo = cu[b], hi = cu[b + 1];
@@ -107,6 +121,8 @@ cudaError_t kvc_launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size
 cudaError_t kvc_launch_advance(kvc_cache* c, int row, int n, cudaStream_t s);
 cudaError_t kvc_launch_reset(kvc_cache* c, int row, cudaStream_t s);
 cudaError_t kvc_launch_set_lengths(kvc_cache* c, const int32_t* kv_len, const int32_t* cu, cudaStream_t s);
+cudaError_t kvc_launch_set_lengths_block(int32_t* block, int B, int cap, const int32_t* kv_len, const int32_t* cu,
+                                         cudaStream_t s);
 cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
                              cudaStream_t s);
 cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,

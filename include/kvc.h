@@ -164,8 +164,9 @@ int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
  * "proposed boundary"].
  *  d_rope (device fp32, [rope_positions][head_dim/2][2]): (cos, sin) of the angle of pair
  *    j at position p; pair j of a head is (x[2j], x[2j+1]) and turns to
- *    (x0 cos - x1 sin, x0 sin + x1 cos), computed in fp32 (fp64 for an F32 store) and
- *    rounded once to the store type.
+ *    (x0 cos - x1 sin, x0 sin + x1 cos).  The store receives the exact value of each
+ *    component for the given x and table entries, rounded once to nearest-even in the
+ *    store type (for finite inputs): the same bits whichever rounding path a lane takes.
  *  Position of token i: CIRCULAR (chunks reserved - 1) * chunk + i; LINEAR the reserved
  *    base + i, or d_slots[i] when given; PACKED i (position within its row).
  * Tokens whose position is outside [0, rope_positions) are not written (K nor V) and
@@ -182,6 +183,36 @@ int kvc_write_rope(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
  *    changed.  Sets each row's kv_len to its length. */
 int kvc_set_lengths(kvc_cache* c, const int32_t* d_kv_len, const int32_t* d_cu_seqlens,
                     void* stream);
+
+/* Length layout shared by several handles [VAR Description: the cu_seqlens_kv of a
+ * length layout are prepared once and cached, then reused by every layer and denoising
+ * step; acceptance row "prepared once per length layout"].  A model with many layers
+ * attending the same ragged text K/V (or the same per-row active prefixes) creates one
+ * layout, sets it once per step, and points every layer's handle at it, instead of one
+ * kvc_set_lengths per layer.
+ *  d_block: caller-owned device memory of kvc_lengths_bytes(batch) bytes, 16-byte
+ *    aligned, in the meta block's layout (error word, per-row kv_len, cu_seqlens);
+ *    kvc_lengths_create enqueues its zeroing on `stream` (no row has a length yet).
+ *  layout: KVC_LINEAR (per-row kv_len) or KVC_PACKED (cu_seqlens); CIRCULAR handles
+ *    take their lengths from their own chunk state (KVC_ERR_UNSUPPORTED).
+ *  capacity: lengths (LINEAR) or the packed total (PACKED) above it are rejected on the
+ *    device as in kvc_set_lengths; every attend checks again against its own store.
+ * kvc_lengths_set takes the same device arrays as kvc_set_lengths, with the same
+ * checks; a bad array sets a bit in the layout's own error word, which kvc_get_error
+ * of any handle using the layout reports (and clears).
+ * kvc_use_lengths(c, L): from now on c's attends (and its PACKED writes) read kv_len /
+ * cu_seqlens from L's block; L = NULL returns c to its own meta block.  L's batch must
+ * equal c's and its capacity must not exceed c's (KVC_ERR_ARG); its layout must be c's
+ * (KVC_ERR_UNSUPPORTED).  Host-side only: it enqueues nothing, and a graph captured
+ * before the call keeps reading what it read when captured.  L must outlive every
+ * handle using it. */
+typedef struct kvc_lengths kvc_lengths;
+size_t kvc_lengths_bytes(int32_t batch);
+int kvc_lengths_create(int32_t batch, int32_t layout, int32_t capacity, void* d_block, void* stream,
+                       kvc_lengths** out);
+int kvc_lengths_set(kvc_lengths* L, const int32_t* d_kv_len, const int32_t* d_cu_seqlens, void* stream);
+int kvc_use_lengths(kvc_cache* c, const kvc_lengths* L);
+int kvc_lengths_destroy(kvc_lengths* L);
 
 /* out[b, i, h, :] = sum_j softmax_j(scale * q[b,i,h,:] . k_j) v_j over row b's
  * valid slots, read in physical order with no gather or roll (unmasked attention
@@ -233,6 +264,16 @@ int kvc_reset(kvc_cache* c, int32_t row, void* stream);
  * tile-claim counters in the workspace are zeroed too, so the next attend starts
  * clean. */
 int kvc_get_error(kvc_cache* c, void* stream, int32_t* bits);
+
+/* Testing hook for the failure path (not for production use).  Every wait inside the
+ * tensor-core and decode attention kernels is bounded (0.5 s): when one runs out, the
+ * kernel stops issuing work, lets its own copies and tensor-core operations in flight
+ * finish, frees its tensor memory, sets KVC_DEV_TIMEOUT and returns, so that the context
+ * stays usable.  With ns > 0, the steady-state waits of c's later attends wait instead
+ * on a barrier that nothing signals, for ns nanoseconds, so that a test can make a wait
+ * run out without any fault or hang; waits while draining are unchanged.  ns = 0 turns
+ * the hook off.  Host-side only. */
+int kvc_debug_stall_waits(kvc_cache* c, uint64_t ns);
 
 /* Free the host handle.  Device buffers stay with the caller. */
 int kvc_destroy(kvc_cache* c);
