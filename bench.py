@@ -268,6 +268,205 @@ def decode_bench(kvc, peaks, per_graph=64, replays=5):
     return res
 
 
+def _events_time(fn, reps):
+    """Seconds per call of fn (which enqueues GPU work on the current stream)."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) * 1e-3 / reps
+
+
+def dit_bench(kvc, peaks, reps=3):
+    """The streaming DiT workload (B2 cond/uncond, H 12, D 128, bf16, chunk 4680, sink
+    4680, window 32760, 10 chunks of which 3 evict, 4 denoising rewrites each; 52.75
+    TFLOP per run): a whole run (reset, then per chunk advance + 4 x (write + attend))
+    launched eagerly and with each chunk's lifecycle replayed from one captured CUDA
+    graph, plus one full-window attend alone."""
+    w = wl.DIT_STREAM
+    cache = kvc.KVCache(w.batch, w.heads, w.kv_heads, w.head_dim, torch.bfloat16, "circular", sink=w.sink,
+                        window=w.window, chunk=w.chunk)
+    sets = [wl.chunk_inputs(w, 0, r, device="cuda") for r in range(w.rewrites)]
+    outs = [torch.empty_like(sets[0][0]) for _ in sets]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+
+    def chunk_body(stream):
+        cache.advance(stream=stream)
+        for (q, k, v), o in zip(sets, outs):
+            cache.write(k, v, stream=stream)
+            cache.attend(q, o, stream=stream)
+
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            cache.reset(stream=side)
+            for _ in range(w.n_chunks):
+                chunk_body(side)
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            chunk_body(side)
+
+        def eager_run():
+            cache.reset(stream=side)
+            for _ in range(w.n_chunks):
+                chunk_body(side)
+
+        def graph_run():
+            cache.reset(stream=side)
+            for _ in range(w.n_chunks):
+                graph.replay()
+
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        res = {}
+        for name, fn in (("eager", eager_run), ("graph", graph_run)):
+            fn()
+            a.record(side)
+            for _ in range(reps):
+                fn()
+            b.record(side)
+            b.synchronize()
+            res[name] = a.elapsed_time(b) * 1e-3 / reps
+        # one attend over the full 32760-slot window (the ring is full after a run)
+        q, _, _ = sets[0]
+        for _ in range(2):
+            cache.attend(q, outs[0], stream=side)
+        a.record(side)
+        for _ in range(reps):
+            cache.attend(q, outs[0], stream=side)
+        b.record(side)
+        b.synchronize()
+        t_full = a.elapsed_time(b) * 1e-3 / reps
+    assert cache.get_error() == 0
+    flops = ring_flops(w)[0]
+    f_full = wl.attention_flops(w.chunk, w.window, w.heads, w.head_dim) * w.batch
+    cache.close()
+    return {"workload": w.name, "tflop_per_run": round(flops / 1e12, 3),
+            "run_ms_eager": round(res["eager"] * 1e3, 3), "run_ms_graph": round(res["graph"] * 1e3, 3),
+            "TFLOP/s": round(flops / res["graph"] / 1e12, 1),
+            "frac": round(flops / res["graph"] / 1e12 / peaks["bf16_sust"], 4),
+            "peak_kind": f"bf16 dense sustained, {peaks['src']}",
+            "full_window_attend": {"ms": round(t_full * 1e3, 4), "TFLOP/s": round(f_full / t_full / 1e12, 1),
+                                   "frac": round(f_full / t_full / 1e12 / peaks["bf16"], 4),
+                                   "peak_kind": f"bf16 dense burst, {peaks['src']}"},
+            "timing": f"whole run x {reps}; graph = one captured chunk (advance + {w.rewrites} x (write + attend)) "
+                      f"replayed per chunk"}
+
+
+def tiny_bench(kvc, reps=20):
+    """The tiny circular workload (fp32, B1 H2 D64, chunk 4, sink 4, window 16, 7 chunks x
+    2 rewrites, then reset): absolute time of a chunk step (advance + 2 x (write +
+    attend)) and of the whole run with its reset, eager and as a replayed graph."""
+    w = wl.TINY_RING
+    cache = kvc.KVCache(w.batch, w.heads, w.kv_heads, w.head_dim, torch.float32, "circular", sink=w.sink,
+                        window=w.window, chunk=w.chunk)
+    sets = [wl.chunk_inputs(w, 0, r, device="cuda") for r in range(w.rewrites)]
+    outs = [torch.empty_like(sets[0][0]) for _ in sets]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+
+    def chunk_body(stream):
+        cache.advance(stream=stream)
+        for (q, k, v), o in zip(sets, outs):
+            cache.write(k, v, stream=stream)
+            cache.attend(q, o, stream=stream)
+
+    with torch.cuda.stream(side):
+        cache.reset(stream=side)
+        for _ in range(w.n_chunks):
+            chunk_body(side)
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            cache.reset(stream=side)
+            for _ in range(w.n_chunks):
+                chunk_body(side)
+        graph.replay()
+
+        def eager_run():
+            cache.reset(stream=side)
+            for _ in range(w.n_chunks):
+                chunk_body(side)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        times = {}
+        for name, fn in (("eager", eager_run), ("graph", graph.replay)):
+            fn()
+            a.record(side)
+            for _ in range(reps):
+                fn()
+            b.record(side)
+            b.synchronize()
+            times[name] = a.elapsed_time(b) * 1e-3 / reps
+    assert cache.get_error() == 0
+    launches = 1 + w.n_chunks * (1 + 2 * w.rewrites)
+    return {"workload": w.name, "run_us_eager": round(times["eager"] * 1e6, 2),
+            "run_us_graph": round(times["graph"] * 1e6, 2),
+            "chunk_step_us_graph": round(times["graph"] / w.n_chunks * 1e6, 2), "launches_per_run": launches,
+            "timing": f"reset + {w.n_chunks} chunks x {w.rewrites} rewrites, {reps} runs; latency-bound "
+                      f"(no roofline fraction)"}
+
+
+def decode_schedule_bench(kvc, peaks, reps=5):
+    """The active-prefix workload as the pages run it (fp16, H 32 / Hkv 8, D 128, a
+    32768-slot store): prefill of 234 tokens (advance, write, causal attend of the 234
+    queries), then 512 decode steps (advance one slot, write its K/V, attend), kv_len
+    235..746.  The 512 steps are one captured graph; tokens/s = 512 / their time."""
+    w = wl.DECODE
+    T, N = wl.DECODE_PROMPT, wl.DECODE_STEPS
+    c = kvc.KVCache(w.batch, w.heads, w.kv_heads, w.head_dim, torch.float16, "linear", capacity=w.capacity)
+    g = torch.Generator(device="cuda").manual_seed(w.seed)
+    qp = torch.randn(1, T, w.heads, w.head_dim, device="cuda", generator=g).half()
+    kp = torch.randn(1, T, w.kv_heads, w.head_dim, device="cuda", generator=g).half()
+    q1 = torch.randn(1, 1, w.heads, w.head_dim, device="cuda", generator=g).half()
+    k1 = torch.randn(1, 1, w.kv_heads, w.head_dim, device="cuda", generator=g).half()
+    op, o1 = torch.empty_like(qp), torch.empty_like(q1)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+
+    def prefill():
+        c.reset(stream=side)
+        c.advance(n_tokens=T, stream=side)
+        c.write(kp, kp, stream=side)
+        c.attend(qp, op, flags=kvc.CAUSAL, stream=side)
+
+    with torch.cuda.stream(side):
+        prefill()
+        for _ in range(3):
+            c.advance(n_tokens=1, stream=side)
+            c.write(k1, k1, stream=side)
+            c.attend(q1, o1, stream=side)
+        side.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            for _ in range(N):
+                c.advance(n_tokens=1, stream=side)
+                c.write(k1, k1, stream=side)
+                c.attend(q1, o1, stream=side)
+        a, b, m = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        t_pre = t_dec = 0.0
+        for _ in range(reps + 1):
+            a.record(side)
+            prefill()
+            m.record(side)
+            graph.replay()
+            b.record(side)
+            b.synchronize()
+            if _ > 0:
+                t_pre += a.elapsed_time(m) * 1e-3 / reps
+                t_dec += m.elapsed_time(b) * 1e-3 / reps
+    assert c.get_error() == 0
+    kv_bytes = sum(2 * (T + i + 1) * w.kv_heads * w.head_dim * 2 for i in range(N))
+    c.close()
+    return {"workload": w.name, "prefill_us": round(t_pre * 1e6, 2), "decode_steps": N,
+            "decode_ms": round(t_dec * 1e3, 4), "tokens_per_s": round(N / t_dec, 1),
+            "us_per_step": round(t_dec / N * 1e6, 3),
+            "kv_GB/s": round(kv_bytes / t_dec / 1e9, 1), "kv_frac": round(kv_bytes / t_dec / 1e9 / peaks["hbm"], 4),
+            "timing": f"prefill eager + {N} steps (advance + write + attend) as one graph, {reps} runs; "
+                      f"kv_len {T + 1}..{T + N}, latency-bound"}
+
+
 def kernel_code_sha256(path):
     """sha256 of a CUDA source with its // comments and blank lines removed: the code a
     capture was taken of (comment edits do not change the kernel)."""
@@ -339,8 +538,49 @@ def cross_bench(kvc, peaks, reps=10, lq=None):
         packed.write(kv, kv)
         padded.set_lengths(kv_len=torch.tensor(lens, dtype=torch.int32, device="cuda"))
         res[name] = {"packed": timed(packed, lens), "kv_len": timed(padded, lens)}
+        if name == "typical":
+            res["metadata"] = metadata_bench(kvc, packed, q, out, lens, reps)
         packed.close()
     return res
+
+
+def metadata_bench(kvc, packed, q, out, lens, reps, layers=40):
+    """The cost of preparing the length metadata, as the pages' cross-attention
+    microbenchmark splits it (_total with the per-call metadata preparation, _kernel
+    without): per attend, (i) the kernel alone over a layout prepared once, (ii) each
+    call copying its cu_seqlens up from pinned host memory and setting them before the
+    attend, (iii) one copy and set per step shared by 40 layers' attends."""
+    shared = kvc.KVLengths(packed.cfg.batch, "packed", packed.cfg.capacity)
+    host_cu = torch.tensor(wl.seqlens_to_cu(lens), dtype=torch.int32).pin_memory()
+    dev_cu = torch.empty_like(host_cu, device="cuda")
+    packed.use_lengths(shared)
+
+    def prep():
+        dev_cu.copy_(host_cu, non_blocking=True)
+        shared.set(cu_seqlens=dev_cu)
+
+    def total():
+        prep()
+        packed.attend(q, out)
+
+    def per_step():
+        prep()
+        for _ in range(layers):
+            packed.attend(q, out)
+
+    prep()
+    for fn in (total, lambda: packed.attend(q, out)):
+        fn()
+    t_kernel = _events_time(lambda: packed.attend(q, out), reps)
+    t_total = _events_time(total, reps)
+    t_step = _events_time(per_step, max(1, reps // 5)) / layers
+    assert packed.get_error() == 0
+    packed.use_lengths(None)
+    return {"kernel_ms": round(t_kernel * 1e3, 4), "total_ms": round(t_total * 1e3, 4),
+            "total_over_kernel": round(t_total / t_kernel, 4),
+            "shared_layout_ms_per_layer": round(t_step * 1e3, 4), "layers": layers,
+            "note": "total = cu_seqlens copied up + kvc_lengths_set + attend, per call; shared = one copy + "
+                    "set per step, read by every layer's attend"}
 
 
 def cpu_oracle_sample(w, budget_s=12.0):
@@ -473,7 +713,25 @@ def ours(args):
     if clocks is not None:
         result["clocks"] = clocks
     result["decode"] = decode_bench(kvc, peaks)
+    result["decode"]["schedule_prefill_512_steps"] = decode_schedule_bench(kvc, peaks)
     result["cross_attention"] = cross_bench(kvc, peaks)
+    result["dit_stream"] = dit_bench(kvc, peaks)
+    result["tiny_ring"] = tiny_bench(kvc)
+    result["next_rows"] = next_rows_bench(kvc, peaks, reps=10)
+    # the RoPE write on this workload's chunk (1.53 GB moved), against the plain write
+    table = wl.rope_table(w.window, w.head_dim).cuda()
+    k0, v0 = inputs[0][1], inputs[0][2]
+    cache.reset()
+    cache.advance()
+    t_plain = _events_time(lambda: cache.write(k0, v0), 5)
+    t_rope = _events_time(lambda: cache.write_rope(k0, v0, table), 5)
+    assert cache.get_error() == 0
+    rope_bytes = write_bytes + w.chunk * (w.head_dim // 2) * 2 * 4
+    result["next_rows"]["write_rope_multi_user_chunk"] = {
+        "us": round(t_rope * 1e6, 2), "GB/s": round(rope_bytes / t_rope / 1e9, 1),
+        "frac": round(rope_bytes / t_rope / 1e9 / peaks["hbm"], 4), "bytes": rope_bytes,
+        "x_plain_write": round(t_rope / t_plain, 3), "plain_write_us": round(t_plain * 1e6, 2)}
+    del table
 
     # end to end through the binding: host (pinned) inputs copied in, output read back.
     # A serving loop pipelines the copies: inputs of the next chunk go up on a copy
@@ -554,11 +812,19 @@ def ours(args):
         b.record(comp)
         b.synchronize()
         down = 3 * out_host[0].numel() * out_host[0].element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+        device_ms = elapsed / args.steps * 1e3
+        copy_ms = (h2d / up + d2h / down) / 1e6
+        e2e_ms = e2e_t / args.steps * 1e3
         result["e2e"] = {"value": round(world * step_flops * args.steps / e2e_t / 1e12, 2), "unit": "TFLOP/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "ms_per_step": round(e2e_t / args.steps * 1e3, 3),
+                         "ms_per_step": round(e2e_ms, 3),
                          "pipelining": "inputs up and outputs down on two copy streams, overlapping compute",
-                         "host_link_GB/s": {"h2d": round(up, 1), "d2h": round(down, 1)}}
+                         "host_link_GB/s": {"h2d": round(up, 1), "d2h": round(down, 1)},
+                         "overlap": {"device_ms_per_step": round(device_ms, 3),
+                                     "copies_alone_ms_per_step": round(copy_ms, 3),
+                                     "serial_ms": round(device_ms + copy_ms, 3),
+                                     "ideal_ms": round(max(device_ms, copy_ms), 3),
+                                     "hidden_frac": round((device_ms + copy_ms - e2e_ms) / min(device_ms, copy_ms), 4)}}
     if rank == 0:
         tf, dt, nrows = cpu_oracle_sample(w)
         result["cpu_baseline"] = {"value": round(tf, 6), "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
