@@ -691,6 +691,15 @@ def ours(args):
         "write": {"GB/s": round(write_gbs, 1), "frac": round(write_gbs / peaks["hbm"], 4),
                   "bytes_per_launch": write_bytes, "us_avg": round(float(np.mean(write_t)) * 1e6, 2)},
     }
+    if args.step_only:
+        clocks = clk.summary()
+        if clocks is not None:
+            result["clocks"] = clocks
+        if rank == 0:
+            print(json.dumps(result), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
     # the per-step copy a chronological store would make (the circular layout skips it)
     scratch = torch.empty(kvc.kvc_roll_scratch_bytes(cache.cfg), dtype=torch.uint8, device="cuda")
     if scratch.numel() > 0:
@@ -955,6 +964,8 @@ def main():
                     help="time only the ragged cross-attention attends and print them (profiling aid)")
     ap.add_argument("--cross-lq", type=int, default=None,
                     help="padded query count of the cross-attention timing (default: the full workload)")
+    ap.add_argument("--step-only", action="store_true",
+                    help="time only the workload step (no extra sections): a profiling aid")
     ap.add_argument("--next-rows", action="store_true",
                     help="time only the RoPE write, the LSE merge and attention with LSE output, and print them")
     args = ap.parse_args()

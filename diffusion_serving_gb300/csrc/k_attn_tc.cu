@@ -116,6 +116,19 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -133,6 +146,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // the abort itself).  `honour_abort` = false is used while draining.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile WaitCtl* w,
                                           bool honour_abort = true) {
+  if (mbar_test_wait(bar, parity)) return true;    // already complete: no flag is read
   if (honour_abort && w->stall) {   // the failure-path test: a wait that nothing ends
     bar = const_cast<uint64_t*>(&w->never);
     parity = 0;
@@ -261,6 +275,21 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Per-warpgroup register split (all four warps of a warpgroup execute it): the pair
+// kernel launches 384 threads x 168 registers = 64,512; warps 0-3 (TMA producers and MMA
+// issuers) give theirs down to 72 and the two softmax warpgroups take 216 each:
+// 128 x 72 + 256 x 216 = 64,512, the launch's total, so every increase is served.  The
+// launcher checks that the compiled kernel does launch with 168 registers per thread
+// (an increase beyond the launch's total would never be served).
+template <uint32_t kRegs> __device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs> __device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 72, kRegsSoftmax = 216;
+static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split above the launch's total");
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -304,16 +333,16 @@ __device__ __forceinline__ float row_max(const uint32_t* sr, int valid) {
 }
 
 // p = 2^(s * c - m) for the first 32 * kChunks columns (0 past `valid` when kMask),
-// packed as 16-bit pairs over the first 64 TMEM columns of the row's S; the P of the
-// chunks past kChunks is stored as 0 (the PV MMA reads all 128).  Returns the row sum of
-// p.  Pairs of columns go through the packed fp32x2 FMA / add.
-template <bool kBf16, bool kMask, int kChunks, bool kTrackMax = false>
+// packed as 16-bit pairs over the first 64 TMEM columns of the row's S; with kZeroRest
+// the P of the chunks past kChunks is stored as 0 (for a PV MMA that reads all 128).
+// Returns the row sum of p.  Pairs of columns go through the packed fp32x2 FMA / add.
+template <bool kBf16, bool kMask, int kChunks, bool kTrackMax = false, bool kZeroRest = true>
 __device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, float c, float m_use, uint32_t s_addr,
                                                 float* raw_max = nullptr) {
   const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
   float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  if (kChunks < 4) {
+  if (kChunks < 4 && kZeroRest) {
     uint32_t zero[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) zero[i] = 0u;
@@ -459,7 +488,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp == 0 || warp == 3) {
+  // the register split comes first in each role's code (so the compiler sizes each role's
+  // code by its own share)
+  if (warp < 4) {
+   regs_dec<kRegsCtl>();
+   if (warp == 0 || warp == 3) {
     // ---------------- TMA producers: warp 0 Q and K, warp 3 V ----------------
     // (two threads, so that a K load never queues behind a V load waiting for a PV)
     if (lane == 0) {
@@ -505,7 +538,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           mbar_wait(kq ? &sm.k_full[j % kStages] : &sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
       }
     }
-  } else if (warp == 1 || warp == 2) {
+   } else {
     // ---------------- MMA issuers: warp 1 for query tile A, warp 2 for tile B ----------------
     // Each issues its tile's chain PV(j), QK(j + 1) from one thread (in order, so QK(j + 1)
     // overwrites S only after PV(j) read P from it); two issuing warps on different
@@ -515,20 +548,35 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     constexpr uint32_t kIdQK = idesc_f16(kBf16 ? 1u : 0u, 0);
     constexpr uint32_t kIdPV = idesc_f16(kBf16 ? 1u : 0u, 1);
     const uint32_t s_col = t ? 128u : 0u, o_col = t ? 384u : 256u;
-    auto issue_qk = [&](int s) {
+    // A short last tile without the causal mask (`rem` slots in range, the same for every
+    // row) is computed only as far as the softmax reads it: QK over 32 * ceil(rem / 32)
+    // slots (MMA N), PV over 16 * ceil(rem / 16) slots (K steps).  The softmax stores P
+    // for those columns only.
+    auto trimmed = [&](int rem) { return !p.causal && rem < kBN; };
+    auto issue_qk = [&](int s, int rem) {
       const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[s]);
+      const uint32_t idesc =
+          trimmed(rem) ? (kIdQK & ~(0x3Fu << 17)) | ((uint32_t)(((rem + 31) / 32) * 32 >> 3) << 17) : kIdQK;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-        mma_ss(tmem + s_col, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdQK, kk > 0);
+        mma_ss(tmem + s_col, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idesc, kk > 0);
       }
     };
-    auto issue_pv = [&](int s, int j) {
+    auto pv_steps = [&](int rem) { return trimmed(rem) ? (rem + 15) / 16 : kBN / 16; };
+    auto issue_pv = [&](int s, int j, int steps) {
       const uint32_t va = smem_u32(sm.v[s]);
+      if (steps == kBN / 16) {
 #pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
-               (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      } else {
+#pragma unroll 1
+        for (int kk = 0; kk < steps; ++kk)
+          mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+      }
     };
     int T = 0, n_items_done = 0;
     RowCache rc;
@@ -542,7 +590,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        issue_qk(s0);
+        issue_qk(s0, I.kv_end);
         mma_commit(&sm.s_full[t]);
         mma_commit(&sm.k_empty[s0]);
         if (I.n_tiles == 1) mma_commit(&sm.q_free);
@@ -555,9 +603,10 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           if (!ok) break;
           const int rem = I.kv_end - j * kBN;
           if (rem < kBN) {
-            // slots past the valid range may hold anything (NaN included): zero those V rows
-            // so that P = 0 there contributes exactly nothing
-            for (int e = lane; e < (kBN - rem) * 2 * 8; e += 32) {
+            // slots past the valid range may hold anything (NaN included): zero the V rows
+            // the PV reads there, so that P = 0 contributes exactly nothing
+            const int rows_read = pv_steps(rem) * 16;
+            for (int e = lane; e < (rows_read - rem) * 2 * 8; e += 32) {
               const int r = rem + e / 16, half = (e / 8) & 1, c = e & 7;
               *reinterpret_cast<uint4*>(sm.v[s] + half * kBoxBytes + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
             }
@@ -581,7 +630,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          issue_pv(s, j);
+          issue_pv(s, j, pv_steps(I.kv_end - j * kBN));
           mma_commit(&sm.v_empty[s]);
           mbar_arrive(&sm.tok[t]);
         }
@@ -590,7 +639,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           if (!ok) break;
           tc_fence_after();
           if (lane == 0) {
-            issue_qk(s1);
+            issue_qk(s1, I.kv_end - (j + 1) * kBN);
             mma_commit(&sm.s_full[t]);
             mma_commit(&sm.k_empty[s1]);
             if (j + 2 == I.n_tiles) mma_commit(&sm.q_free);   // that was this item's last QK
@@ -609,8 +658,16 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       mbar_wait(&sm.drain[t], 0, abort, false);
     }
     __syncwarp();
-  } else if (warp >= 4) {
+   }
+  } else {
+    regs_inc<kRegsSoftmax>();
     // ---------------- softmax (one query row per thread) ----------------
+    // The epilogue of an item (O / l to global memory) is deferred into the next item:
+    // the warp first turns that item's first S tile into P, then reads the previous O out
+    // of TMEM, and only then signals P-ready, which also tells the issuer that O is free
+    // for the next item's first PV.  The wait for the previous item's last PV is thereby
+    // spent on useful work, and the conversion and stores of the previous O run while the
+    // tensor pipe works on the new item.
     const int t = (warp - 4) >> 2;          // query tile A or B
     const int quad = warp & 3;              // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;         // row within the tile
@@ -622,6 +679,56 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     int T = 0, n_items_done = 0;
     RowCache rc;
     bool ok = true;
+    // the item whose output is still in O: its head, batch row, first row of this warp, this
+    // thread's query row, and the row's running max and sum
+    bool pend = false;
+    int pend_b = 0, pend_h = 0, pend_grow = 0, pend_row = 0;
+    float pend_m = 0.f, pend_l = 0.f;
+    // O of the pending item -> registers (normalised, packed 16-bit); waits for its last PV
+    auto o_read = [&](uint32_t* pk) {
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (n_items_done - 1) & 1, abort));
+      if (!ok) return;
+      tc_fence_after();
+      const float inv = pend_l > 0.f ? 1.f / pend_l : 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t orow[32];
+        tmem_ld32(o_addr + q4 * 32, orow);
+        tmem_ld_wait();
+        reg_fence32(orow);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[2 * i]), __uint_as_float(orow[2 * i + 1])),
+                                      make_float2(inv, inv));
+          pk[16 * q4 + i] = pack2<kBf16>(y.x, y.y);
+        }
+      }
+    };
+    // packed O rows -> 64-byte-swizzled staging (16-byte chunk c of row r at chunk
+    // c ^ ((r >> 1) & 3), conflict-free) -> one TMA store per 32 columns; rows past n_q
+    // are clipped by the map.  Also the LSE of the row.
+    auto o_store = [&](const uint32_t* pk) {
+      if (p.lse != nullptr && pend_row < p.n_q)   // m and l are in the exp2 domain of scale * q.k
+        p.lse[((int64_t)pend_b * p.n_q + pend_row) * g.H + pend_h] =
+            pend_l > 0.f ? (pend_m + log2f(pend_l)) * 0.6931471805599453f : -INFINITY;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint8_t* buf = stage + (q4 & 1) * kStageBytes;
+        if (lane == 0) bulk_wait_read1();              // the store that last read buf is done with it
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
+              make_uint4(pk[16 * q4 + 4 * i], pk[16 * q4 + 4 * i + 1], pk[16 * q4 + 4 * i + 2],
+                         pk[16 * q4 + 4 * i + 3]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&tm_o, buf, q4 * 32, pend_h, pend_grow, pend_b);
+          bulk_commit();
+        }
+      }
+    };
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       Item I;
       if (!item_geom(item, pairs, p, meta, rc, &I)) continue;
@@ -637,7 +744,8 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (p.causal) valid = min(valid, qpos - j * kBN + 1);
         // One pass over the tile's S row: kChunks 32-column chunks hold slots in range
         // (fewer than 4 only on a short last tile without the causal mask, where
-        // `valid` is the same for every row); kMask masks columns past `valid`.
+        // `valid` is the same for every row and the MMAs cover only those chunks);
+        // kMask masks columns past `valid`.
         auto tile = [&](auto chunks, auto mask) {
           constexpr int kC = decltype(chunks)::value;
           constexpr bool kM = decltype(mask)::value;
@@ -651,8 +759,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           bool rescale = m_tile > m_ref + kRescaleThreshold;
           const float m_new = rescale ? m_tile : m_ref;
           const float m_use = m_new == -INFINITY ? 0.f : m_new;
+          const float alpha = rescale && j > 0 ? ex2(m_ref - m_use) : 1.f;
+          m_ref = m_new;
+          // P first (the S row's registers are free after it), then O *= alpha: both land
+          // before this tile's P-ready, which the PV of the tile waits for
+          l = l * alpha + exp_pack_store<kBf16, kM, kC, false, false>(sr, valid, c, m_use, s_addr);
           if (__any_sync(0xffffffffu, rescale) && j > 0) {
-            const float alpha = rescale ? ex2(m_ref - m_use) : 1.f;
 #pragma unroll 1
             for (int q4 = 0; q4 < 4; ++q4) {
               uint32_t orow[32];
@@ -668,11 +780,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
               }
               tmem_st32(o_addr + q4 * 32, orow);
             }
-            tmem_st_wait();
-            l *= alpha;
           }
-          m_ref = m_new;
-          l += exp_pack_store<kBf16, kM, kC>(sr, valid, c, m_use, s_addr);
         };
         using C1 = std::integral_constant<int, 1>;
         using C2 = std::integral_constant<int, 2>;
@@ -694,59 +802,38 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           tile(C3{}, Masked{});
         }
         tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_ready[t]);
-      }
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], n_items_done & 1, abort));
-      if (!ok) break;
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      if (p.lse != nullptr && row < p.n_q)   // m_ref and l are in the exp2 domain of scale * q.k
-        p.lse[((int64_t)I.b * p.n_q + row) * g.H + I.h] =
-            l > 0.f ? (m_ref + log2f(l)) * 0.6931471805599453f : -INFINITY;
-      // O rows -> 64-byte-swizzled staging (16-byte chunk c of row r at chunk c ^ ((r >> 1) & 3),
-      // conflict-free) -> one TMA store per 32 columns; rows past n_q are clipped by the map
-      const int grow = I.row_a + t * kBM + quad * 32;    // first query row of this warp
-#pragma unroll 1
-      for (int q2 = 0; q2 < 2; ++q2) {                  // 64 columns per TMEM round trip
-        uint32_t orow[64];
-        tmem_ld32(o_addr + q2 * 64, orow);
-        tmem_ld32(o_addr + q2 * 64 + 32, orow + 32);
-        tmem_ld_wait();
-        reg_fence32(orow);
-        reg_fence32(orow + 32);
-#pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int q4 = 2 * q2 + c2;
-          const uint32_t* oc = orow + 32 * c2;
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 y = __fmul2_rn(make_float2(__uint_as_float(oc[2 * i]), __uint_as_float(oc[2 * i + 1])),
-                                        make_float2(inv, inv));
-            pk[i] = pack2<kBf16>(y.x, y.y);
-          }
-          uint8_t* buf = stage + c2 * kStageBytes;
-          if (lane == 0) bulk_wait_read1();              // the store that last read buf is done with it
+        if (j == 0 && pend) {
+          // the previous item's O leaves TMEM before this P-ready lets the first PV of this
+          // item overwrite it
+          uint32_t pk[64];
+          o_read(pk);
+          if (!ok) break;
+          tc_fence_before();
           __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
-                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          fence_proxy_async();
+          if (lane == 0) mbar_arrive(&sm.p_ready[t]);
+          o_store(pk);
+          pend = false;
+        } else {
+          tc_fence_before();
           __syncwarp();
-          if (lane == 0) {
-            tma_store_4d(&tm_o, buf, q4 * 32, I.h, grow, I.b);
-            bulk_commit();
-          }
+          if (lane == 0) mbar_arrive(&sm.p_ready[t]);
         }
       }
-      // O of this item has been read: the issuer may overwrite it once this warp's next
-      // P-ready arrives (program order), so no separate signal is needed
-      tc_fence_before();
+      if (!ok) break;
+      pend = true;
+      pend_b = I.b;
+      pend_h = I.h;
+      pend_grow = I.row_a + t * kBM + quad * 32;
+      pend_row = row;
+      pend_m = m_ref;
+      pend_l = l;
       T += I.n_tiles;
       ++n_items_done;
+    }
+    if (ok && pend) {
+      uint32_t pk[64];
+      o_read(pk);
+      if (ok) o_store(pk);
     }
     if (lane == 0) bulk_wait_all();                      // staging stays live until the stores land
     __syncwarp();
@@ -1210,6 +1297,20 @@ bool kvc_tc_make_kv_maps(kvc_cache* c) {
   return true;
 }
 
+namespace {
+// The pair kernel's register split needs every thread launched with kRegsLaunch registers.
+bool pair_regs_ok() {
+  static int ok = -1;
+  if (ok < 0) {
+    cudaFuncAttributes a{}, b{};
+    ok = cudaFuncGetAttributes(&a, k_attn_tc<true>) == cudaSuccess &&
+         cudaFuncGetAttributes(&b, k_attn_tc<false>) == cudaSuccess && a.numRegs == (int)kRegsLaunch &&
+         b.numRegs == (int)kRegsLaunch;
+  }
+  return ok == 1;
+}
+}  // namespace
+
 cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
                                cudaStream_t s) {
   const kvc_config& cfg = c->cfg;
@@ -1231,6 +1332,7 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
   // stores run the one-tile kernel, whose triple-buffered S keeps the tensor pipe fed
   // (measured crossover between 512 and 1024 slots).
   if (c->cap <= kShortKv) {
+    if (!pair_regs_ok()) return cudaErrorInvalidConfiguration;
     const int64_t items = (int64_t)((n_q + 2 * kBM - 1) / (2 * kBM)) * cfg.heads * cfg.batch;
     if (items > INT32_MAX) return cudaErrorInvalidValue;
     dim3 grid((unsigned)(items < c->num_sms ? items : c->num_sms));
