@@ -371,6 +371,50 @@ k_write_rope(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uin
   }
 }
 
+// Append to a LINEAR store in one launch: kvc_advance(row -1, n) and the write of the
+// reserved chunk together, for a decode step's few tokens (the fish-speech PR "pass only
+// active KV cache prefix to SDPA", "Change": decode step i stores its token at T + i and
+// attends T + i + 1 slots).  One block: every row's fill count is read first, the rows
+// are copied to slots filled_b + i, and only then is the meta block advanced, so no warp
+// reads a count another has already moved.  A row that would pass its capacity sets
+// KVC_DEV_OVERFLOW and is left unchanged, as kvc_advance does.
+constexpr int kAppendMaxRows = 1024;
+
+__global__ void __launch_bounds__(kWriteThreads)
+k_append(const uint4* __restrict__ ksrc, const uint4* __restrict__ vsrc, uint4* __restrict__ kdst,
+         uint4* __restrict__ vdst, int32_t* __restrict__ meta, int B, int n, int row_vecs, int cap) {
+  __shared__ int s_base[kAppendMaxRows];
+  kvc_pdl_wait();
+  kvc_pdl_release();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int filled = meta[kvc_meta_row(b) + KVC_ROW_FILLED];
+    const bool ok = filled >= 0 && (int64_t)filled + n <= cap;
+    if (!ok) atomicOr(meta + KVC_META_ERR, KVC_DEV_OVERFLOW);
+    s_base[b] = ok ? filled : -1;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int rows = 2 * B * n;
+  for (int r = threadIdx.x >> 5; r < rows; r += blockDim.x >> 5) {
+    const int t = r >= B * n;
+    const int e = r - (t ? B * n : 0);
+    const int b = e / n, i = e - b * n;
+    if (s_base[b] < 0) continue;
+    const uint4* src = (t ? vsrc : ksrc) + (int64_t)e * row_vecs;
+    uint4* dst = (t ? vdst : kdst) + ((int64_t)b * cap + s_base[b] + i) * row_vecs;
+    for (int v = lane; v < row_vecs; v += 32) dst[v] = __ldg(src + v);
+  }
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    if (s_base[b] < 0) continue;
+    int32_t* m = meta + kvc_meta_row(b);
+    m[KVC_ROW_CHUNKS] += 1;
+    m[KVC_ROW_BASE] = s_base[b];
+    m[KVC_ROW_FILLED] = s_base[b] + n;
+    m[KVC_ROW_KVLEN] = s_base[b] + n;
+  }
+}
+
 // Comparator for measurement, not on the path: the copy a chronological sink + window
 // store makes once per chunk step (flashdreams issue "add an opt-in circular KV policy
 // for streaming attention", "current path": the retained keys and values are cloned and
@@ -455,6 +499,19 @@ cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, in
   if (g.dtype == KVC_F16) return KVC_WR(__half);
   return KVC_WR(__nv_bfloat16);
 #undef KVC_WR
+}
+
+// One block moves ~100 GB/s: the single launch pays off for a decode step's bytes only.
+bool kvc_append_fits(const kvc_cache* c, int n) {
+  const int64_t bytes = 2LL * c->cfg.batch * n * c->cfg.kv_heads * c->cfg.head_dim * c->eb;
+  return c->cfg.batch <= kAppendMaxRows && bytes <= (128 << 10);
+}
+
+cudaError_t kvc_launch_append(kvc_cache* c, const void* k, const void* v, int n, cudaStream_t s) {
+  const kvc_config& g = c->cfg;
+  const int row_vecs = g.kv_heads * g.head_dim * c->eb / 16;
+  return kvc_launch_pdl(k_append, dim3(1), dim3(kWriteThreads), 0, s, (const uint4*)k, (const uint4*)v,
+                        (uint4*)c->k, (uint4*)c->v, c->meta, g.batch, n, row_vecs, c->cap);
 }
 
 cudaError_t kvc_launch_roll(kvc_cache* c, void* scratch, cudaStream_t s) {

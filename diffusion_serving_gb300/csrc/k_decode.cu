@@ -204,6 +204,25 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   const int hq = lane >> 2;          // head row of this lane in the MMA fragments (real if < G)
   const int quad = lane & 3;         // column pair within the fragments
 
+  // Set-up that touches no global memory runs before the wait for the previous kernel
+  // (programmatic dependent launch): the barriers, and the TMA descriptors fetched.
+  if (threadIdx.x < kStages) {
+    mbar_init(&full[threadIdx.x], 1);
+    mbar_init(&empty[threadIdx.x], kWarps);
+  }
+  if (threadIdx.x == 0) {
+    s_wc.abort = 0;
+    s_wc.stall = stall_ns > 0;
+    s_wc.limit_ns = stall_ns > 0 ? stall_ns : kTimeoutNs;
+    mbar_init(&s_wc.never, 1);
+  }
+  if (threadIdx.x == kWarps * 32) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_k) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(&tm_v) : "memory");
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  __syncthreads();
+
   kvc_pdl_wait();
   kvc_pdl_release();
   int row0 = 0, len = 0;
@@ -225,18 +244,6 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   int* tickets = reinterpret_cast<int*>(ws_ml + (int64_t)pairs * nsplit * G * 2);  // [pairs]
   int* claims = tickets + pairs;                                 // [pairs]
 
-  if (threadIdx.x < kStages) {
-    mbar_init(&full[threadIdx.x], 1);
-    mbar_init(&empty[threadIdx.x], kWarps);
-  }
-  if (threadIdx.x == 0) {
-    s_wc.abort = 0;
-    s_wc.stall = stall_ns > 0;
-    s_wc.limit_ns = stall_ns > 0 ? stall_ns : kTimeoutNs;
-    mbar_init(&s_wc.never, 1);
-  }
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  __syncthreads();
   volatile WaitCtl* abort = &s_wc;
 
   if (warp == kWarps) {

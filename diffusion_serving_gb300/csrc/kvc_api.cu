@@ -211,6 +211,17 @@ int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, cons
   return launched(kvc_launch_write(c, k, v, n_tokens, d_slots, as_stream(stream)));
 }
 
+int kvc_append(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, void* stream) {
+  if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;
+  if (c->cfg.layout != KVC_LINEAR) return KVC_ERR_UNSUPPORTED;
+  if (n_tokens > c->cap || write_rows_overflow(c, n_tokens)) return KVC_ERR_RANGE;
+  cudaStream_t s = as_stream(stream);
+  if (kvc_append_fits(c, n_tokens)) return launched(kvc_launch_append(c, k, v, n_tokens, s));
+  const cudaError_t e = kvc_launch_advance(c, -1, n_tokens, s);
+  if (e != cudaSuccess) return KVC_ERR_CUDA;
+  return launched(kvc_launch_write(c, k, v, n_tokens, nullptr, s));
+}
+
 int kvc_write_rope(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, const int32_t* d_slots,
                    const float* d_rope, int32_t rope_positions, void* stream) {
   if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;

@@ -128,6 +128,9 @@ cudaError_t kvc_launch_write(kvc_cache* c, const void* k, const void* v, int n, 
 cudaError_t kvc_launch_write_rope(kvc_cache* c, const void* k, const void* v, int n, const int32_t* slots,
                                   const float* rope, int rope_positions, cudaStream_t s);
 cudaError_t kvc_launch_roll(kvc_cache* c, void* scratch, cudaStream_t s);
+// One-launch append (reserve + write) of n tokens per row; only where kvc_append_fits.
+bool kvc_append_fits(const kvc_cache* c, int n);
+cudaError_t kvc_launch_append(kvc_cache* c, const void* k, const void* v, int n, cudaStream_t s);
 cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
                                  cudaStream_t s);
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, bool fixed_tiles, cudaStream_t s);

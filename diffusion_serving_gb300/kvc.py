@@ -58,6 +58,7 @@ def _load():
         "kvc_advance": (ctypes.c_int, [P, I32, I32, P]),
         "kvc_write": (ctypes.c_int, [P, P, P, I32, P, P]),
         "kvc_write_rope": (ctypes.c_int, [P, P, P, I32, P, P, I32, P]),
+        "kvc_append": (ctypes.c_int, [P, P, P, I32, P]),
         "kvc_set_lengths": (ctypes.c_int, [P, P, P, P]),
         "kvc_attend": (ctypes.c_int, [P, P, P, I32, U32, P]),
         "kvc_attend_lse": (ctypes.c_int, [P, P, P, P, I32, U32, P]),
@@ -149,6 +150,10 @@ def kvc_advance(h: int, row: int = -1, n_tokens: int = 0, stream=None) -> None:
 
 def kvc_write(h: int, k, v, n_tokens: int, slots=None, stream=None) -> None:
     _check(_lib.kvc_write(h, _ptr(k), _ptr(v), n_tokens, _ptr(slots), _stream(stream)), "kvc_write")
+
+
+def kvc_append(h: int, k, v, n_tokens: int, stream=None) -> None:
+    _check(_lib.kvc_append(h, _ptr(k), _ptr(v), n_tokens, _stream(stream)), "kvc_append")
 
 
 def kvc_write_rope(h: int, k, v, n_tokens: int, rope, rope_positions: int, slots=None, stream=None) -> None:
@@ -330,6 +335,11 @@ class KVCache:
     def write(self, k, v, slots=None, stream=None):
         self._check_kv(k, v)
         kvc_write(self.handle, k, v, k.shape[1], slots, stream)
+
+    def append(self, k, v, stream=None):
+        """Reserve k.shape[1] slots after those filled (LINEAR) and write k, v there."""
+        self._check_kv(k, v)
+        kvc_append(self.handle, k, v, k.shape[1], stream)
 
     def write_rope(self, k, v, rope, slots=None, stream=None):
         """Write with K rotated by the (cos, sin) table ``rope`` [positions, D/2, 2] fp32."""

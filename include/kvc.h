@@ -158,6 +158,18 @@ int kvc_advance(kvc_cache* c, int32_t row, int32_t n_tokens, void* stream);
 int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
               const int32_t* d_slots, void* stream);
 
+/* Append n_tokens rows of K and V (device, [B, n_tokens, Hkv, D]) to every row of a
+ * LINEAR store: the same as kvc_advance(c, -1, n_tokens) followed by
+ * kvc_write(c, k, v, n_tokens, NULL), in one launch when the K and V bytes appended are
+ * at most 128 KiB (a decode step: the new token of each row goes to slot kv_len and the
+ * row then attends kv_len + 1 slots [PFX "Change"]), as those two launches otherwise.  Slots come from
+ * the meta block on the device, so a captured step appends at the right place on every
+ * replay.  A row that would pass its capacity sets KVC_DEV_OVERFLOW and is left
+ * unchanged.  Errors: KVC_ERR_UNSUPPORTED for CIRCULAR / PACKED (whose slots are
+ * reserved per chunk or come from cu_seqlens), KVC_ERR_RANGE for n_tokens above the
+ * capacity, KVC_ERR_ARG, KVC_ERR_CUDA. */
+int kvc_append(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, void* stream);
+
 /* kvc_write with RoPE fused into the K half: each K row is rotated at its absolute
  * position before it is stored; V rows are copied unchanged.  Keys stored in a circular
  * cache must carry their absolute-position rotation, applied before the write [RING

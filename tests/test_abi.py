@@ -11,7 +11,7 @@ from diffusion_serving_gb300 import kvc
 
 def test_library_exports_every_declared_function():
     names = kvc.header_functions()
-    assert len(names) == 23
+    assert len(names) == 24
     for n in names:
         assert hasattr(kvc._lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", kvc.LIB_PATH], capture_output=True, text=True).stdout

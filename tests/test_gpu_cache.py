@@ -11,6 +11,7 @@ import pytest
 import torch
 
 from oracle import kvc_oracle as orc
+from tests.helpers import assert_close, to64
 
 pytestmark = pytest.mark.gpu
 
@@ -244,3 +245,82 @@ def test_roll_comparator_matches_chronological_copy(dtype):
     want_v = orc.roll_left(bits(before_v).numpy(), S, W, C)
     assert np.array_equal(bits(cache.k_store.cpu()).numpy(), want_k)
     assert np.array_equal(bits(cache.v_store.cpu()).numpy(), want_v)
+
+
+@pytest.mark.parametrize("n", [1, 3, 30, 300])
+def test_append_equals_advance_then_write(n):
+    """kvc_append (one launch for a decode step's few tokens, the advance + write pair
+    for appends of more than 128 KiB) leaves the same store bytes and row state as kvc_advance followed by
+    kvc_write."""
+    B, Hkv, D, cap = 2, 8, 128, 1024
+    a = kvc.KVCache(B, 32, Hkv, D, torch.float16, "linear", capacity=cap)
+    w = kvc.KVCache(B, 32, Hkv, D, torch.float16, "linear", capacity=cap)
+    for c in (a, w):
+        c.k_store.zero_()
+        c.v_store.zero_()
+    g = torch.Generator(device="cuda").manual_seed(n)
+    for step in range(3):
+        k = torch.randn(B, n, Hkv, D, device="cuda", generator=g).half()
+        v = torch.randn(B, n, Hkv, D, device="cuda", generator=g).half()
+        a.append(k, v)
+        w.advance(n_tokens=n)
+        w.write(k, v)
+        assert a.row_state() == w.row_state()
+    assert torch.equal(bits(a.k_store), bits(w.k_store)) and torch.equal(bits(a.v_store), bits(w.v_store))
+    assert a.row_state()[0] == [3, 2 * n, 3 * n, 3 * n]
+    assert a.get_error() == 0 and w.get_error() == 0
+
+
+def test_append_past_capacity_is_reported_and_skipped():
+    cap = 8
+    c = kvc.KVCache(1, 2, 2, 64, torch.bfloat16, "linear", capacity=cap)
+    k = torch.randn(1, 3, 2, 64, device="cuda").bfloat16()
+    c.append(k, k)
+    c.append(k, k)
+    before = c.row_state()
+    c.append(k, k)                                   # 6 + 3 > 8
+    assert c.get_error() == kvc.DEV_OVERFLOW
+    assert c.row_state() == before
+    ring = kvc.KVCache(1, 2, 2, 64, torch.bfloat16, "circular", sink=4, window=16, chunk=4)
+    with pytest.raises(kvc.KvcError) as e:
+        ring.append(k[:, :1].contiguous(), k[:, :1].contiguous())
+    assert e.value.code == kvc.ERR_UNSUPPORTED
+
+
+def test_captured_append_attend_decode_steps_match_the_oracle():
+    """A decode step (append the token's K/V, attend) captured once and replayed: each
+    replay appends at the next slot and attends the whole prefix (fish-speech PR, "Change")."""
+    B, H, Hkv, D, cap, T = 1, 32, 8, 128, 4096, 234
+    c = kvc.KVCache(B, H, Hkv, D, torch.float16, "linear", capacity=cap)
+    orc_c = orc.ChronoCache(B, Hkv, D, orc.LINEAR, capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    kp = torch.randn(B, T, Hkv, D, device="cuda", generator=g).half()
+    vp = torch.randn(B, T, Hkv, D, device="cuda", generator=g).half()
+    c.append(kp, vp)
+    orc_c.advance(n_tokens=T)
+    orc_c.write(to64(kp), to64(vp))
+    k1 = torch.empty(B, 1, Hkv, D, device="cuda").half()
+    v1 = torch.empty_like(k1)
+    q1 = torch.empty(B, 1, H, D, device="cuda").half()
+    o1 = torch.empty_like(q1)
+    q1.zero_()
+    c.attend(q1, o1)                                 # the decode kernel's first launch, outside capture
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        c.append(k1, v1, stream=side)
+        c.attend(q1, o1, stream=side)
+    for i in range(20):
+        for t in (k1, v1, q1):
+            t.normal_(generator=g)
+        graph.replay()
+        torch.cuda.synchronize()
+        orc_c.advance(n_tokens=1)
+        orc_c.write(to64(k1), to64(v1))
+        kk, vv = orc_c.keys_values(0)
+        assert kk.shape[0] == T + i + 1
+        assert_close(o1[0], orc.attend(to64(q1[0]), kk, vv), f"step {i}")
+    assert c.row_state()[0][3] == T + 20
+    assert c.get_error() == 0
