@@ -662,12 +662,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   } else {
     regs_inc<kRegsSoftmax>();
     // ---------------- softmax (one query row per thread) ----------------
-    // The epilogue of an item (O / l to global memory) is deferred into the next item:
-    // the warp first turns that item's first S tile into P, then reads the previous O out
-    // of TMEM, and only then signals P-ready, which also tells the issuer that O is free
-    // for the next item's first PV.  The wait for the previous item's last PV is thereby
-    // spent on useful work, and the conversion and stores of the previous O run while the
-    // tensor pipe works on the new item.
+    // The epilogue of an item (O / l to global memory) runs at the start of the next
+    // item, while that item's Q tiles are still loading: the warp reads the previous O
+    // out of TMEM (once its last PV is done), stores it, and only then waits for the new
+    // item's first S tile.  Its first P-ready, which follows in program order, also tells
+    // the issuer that O is free for the new item's first PV.
     const int t = (warp - 4) >> 2;          // query tile A or B
     const int quad = warp & 3;              // TMEM lane quadrant of this warp
     const int r = quad * 32 + lane;         // row within the tile
@@ -684,15 +683,21 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     bool pend = false;
     int pend_b = 0, pend_h = 0, pend_grow = 0, pend_row = 0;
     float pend_m = 0.f, pend_l = 0.f;
-    // O of the pending item -> registers (normalised, packed 16-bit); waits for its last PV
-    auto o_read = [&](uint32_t* pk) {
+    // The pending item's output: once its last PV is done, O / l leaves TMEM 32 columns at
+    // a time through 64-byte-swizzled staging (16-byte chunk c of row r at chunk
+    // c ^ ((r >> 1) & 3), conflict-free) and one TMA store per 32 columns; rows past n_q
+    // are clipped by the map.  Also the LSE of the row.
+    auto o_flush = [&]() {
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (n_items_done - 1) & 1, abort));
       if (!ok) return;
       tc_fence_after();
       const float inv = pend_l > 0.f ? 1.f / pend_l : 0.f;
-#pragma unroll
+      if (p.lse != nullptr && pend_row < p.n_q)   // m and l are in the exp2 domain of scale * q.k
+        p.lse[((int64_t)pend_b * p.n_q + pend_row) * g.H + pend_h] =
+            pend_l > 0.f ? (pend_m + log2f(pend_l)) * 0.6931471805599453f : -INFINITY;
+#pragma unroll 1
       for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t orow[32];
+        uint32_t orow[32], pk[16];
         tmem_ld32(o_addr + q4 * 32, orow);
         tmem_ld_wait();
         reg_fence32(orow);
@@ -700,27 +705,15 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         for (int i = 0; i < 16; ++i) {
           const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[2 * i]), __uint_as_float(orow[2 * i + 1])),
                                       make_float2(inv, inv));
-          pk[16 * q4 + i] = pack2<kBf16>(y.x, y.y);
+          pk[i] = pack2<kBf16>(y.x, y.y);
         }
-      }
-    };
-    // packed O rows -> 64-byte-swizzled staging (16-byte chunk c of row r at chunk
-    // c ^ ((r >> 1) & 3), conflict-free) -> one TMA store per 32 columns; rows past n_q
-    // are clipped by the map.  Also the LSE of the row.
-    auto o_store = [&](const uint32_t* pk) {
-      if (p.lse != nullptr && pend_row < p.n_q)   // m and l are in the exp2 domain of scale * q.k
-        p.lse[((int64_t)pend_b * p.n_q + pend_row) * g.H + pend_h] =
-            pend_l > 0.f ? (pend_m + log2f(pend_l)) * 0.6931471805599453f : -INFINITY;
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
         uint8_t* buf = stage + (q4 & 1) * kStageBytes;
         if (lane == 0) bulk_wait_read1();              // the store that last read buf is done with it
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
-              make_uint4(pk[16 * q4 + 4 * i], pk[16 * q4 + 4 * i + 1], pk[16 * q4 + 4 * i + 2],
-                         pk[16 * q4 + 4 * i + 3]);
+              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
@@ -735,6 +728,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       const int row = I.row_a + t * kBM + r;   // query row within the chunk
       const int qpos = I.qpos0 + row;
       float m_ref = -INFINITY, l = 0.f;
+      if (pend) {
+        o_flush();
+        if (!ok) break;
+        pend = false;
+      }
       for (int j = 0; j < I.n_tiles; ++j) {
         const int Tj = T + j;
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], Tj & 1, abort));
@@ -802,22 +800,9 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           tile(C3{}, Masked{});
         }
         tmem_st_wait();
-        if (j == 0 && pend) {
-          // the previous item's O leaves TMEM before this P-ready lets the first PV of this
-          // item overwrite it
-          uint32_t pk[64];
-          o_read(pk);
-          if (!ok) break;
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.p_ready[t]);
-          o_store(pk);
-          pend = false;
-        } else {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.p_ready[t]);
-        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_ready[t]);
       }
       if (!ok) break;
       pend = true;
@@ -830,11 +815,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       T += I.n_tiles;
       ++n_items_done;
     }
-    if (ok && pend) {
-      uint32_t pk[64];
-      o_read(pk);
-      if (ok) o_store(pk);
-    }
+    if (ok && pend) o_flush();
     if (lane == 0) bulk_wait_all();                      // staging stays live until the stores land
     __syncwarp();
   }
