@@ -986,12 +986,18 @@ def main():
                     help="padded query count of the cross-attention timing (default: the full workload)")
     ap.add_argument("--step-only", action="store_true",
                     help="time only the workload step (no extra sections): a profiling aid")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="time only the decode attends and steps, and print them (profiling aid)")
     ap.add_argument("--next-rows", action="store_true",
                     help="time only the RoPE write, the LSE merge and attention with LSE output, and print them")
     args = ap.parse_args()
     if args.next_rows:
         from diffusion_serving_gb300 import kvc
         print(json.dumps({"next_rows": next_rows_bench(kvc, load_peaks(), reps=max(args.steps, 5))}))
+        return
+    if args.decode_only:
+        from diffusion_serving_gb300 import kvc
+        print(json.dumps({"decode": decode_bench(kvc, load_peaks())}))
         return
     if args.cross_only:
         from diffusion_serving_gb300 import kvc
