@@ -63,6 +63,7 @@ constexpr uint32_t kTileBytes = 2 * kBoxBytes;       // 128 dims
 constexpr uint32_t kStageBytes = 32 * 32 * 2;        // 32 rows x 32 dims, 16-bit
 constexpr uint64_t kTimeoutNs = 500000000ull;   // 0.5 s; a healthy wait is microseconds
 constexpr float kRescaleThreshold = 8.0f;            // log2 units
+constexpr float kRescaleSum = 256.0f;                // 2^kRescaleThreshold
 
 // Per-CTA abort flag and the limit of its steady-state waits (kTimeoutNs, or the testing
 // hook's stall_ns); waits while draining after an abort always use kTimeoutNs.
@@ -277,8 +278,8 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // Per-warpgroup register split (all four warps of a warpgroup execute it): the pair
 // kernel launches 384 threads x 168 registers = 64,512; warps 0-3 (TMA producers and MMA
-// issuers) give theirs down to 72 and the two softmax warpgroups take 216 each:
-// 128 x 72 + 256 x 216 = 64,512, the launch's total, so every increase is served.  The
+// issuers) give theirs down to 80 and the two softmax warpgroups take 208 each:
+// 128 x 80 + 256 x 208 = 63,488, within the launch's total, so every increase is served.  The
 // launcher checks that the compiled kernel does launch with 168 registers per thread
 // (an increase beyond the launch's total would never be served).
 template <uint32_t kRegs> __device__ __forceinline__ void regs_dec() {
@@ -287,7 +288,7 @@ template <uint32_t kRegs> __device__ __forceinline__ void regs_dec() {
 template <uint32_t kRegs> __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
-constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 72, kRegsSoftmax = 216;
+constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 80, kRegsSoftmax = 208;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split above the launch's total");
 
 __device__ __forceinline__ float ex2(float x) {
@@ -336,12 +337,10 @@ __device__ __forceinline__ float row_max(const uint32_t* sr, int valid) {
 // packed as 16-bit pairs over the first 64 TMEM columns of the row's S; with kZeroRest
 // the P of the chunks past kChunks is stored as 0 (for a PV MMA that reads all 128).
 // Returns the row sum of p.  Pairs of columns go through the packed fp32x2 FMA / add.
-template <bool kBf16, bool kMask, int kChunks, bool kTrackMax = false, bool kZeroRest = true>
-__device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, float c, float m_use, uint32_t s_addr,
-                                                float* raw_max = nullptr) {
+template <bool kBf16, bool kMask, int kChunks, bool kZeroRest = true>
+__device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, float c, float m_use, uint32_t s_addr) {
   const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_use, -m_use);
   float2 sum[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   if (kChunks < 4 && kZeroRest) {
     uint32_t zero[16];
 #pragma unroll
@@ -361,20 +360,11 @@ __device__ __forceinline__ float exp_pack_store(const uint32_t* sr, int valid, f
         x0 = c0 < valid ? x0 : 0.f;
         x1 = c0 + 1 < valid ? x1 : 0.f;
       }
-      if (kTrackMax) {
-        float s0 = __uint_as_float(sr[c0]), s1 = __uint_as_float(sr[c0 + 1]);
-        if (kMask) {
-          s0 = c0 < valid ? s0 : -INFINITY;
-          s1 = c0 + 1 < valid ? s1 : -INFINITY;
-        }
-        mx[i & 3] = fmax3(mx[i & 3], s0, s1);
-      }
       sum[i & 1] = __fadd2_rn(sum[i & 1], make_float2(x0, x1));
       pk[i] = pack2<kBf16>(x0, x1);
     }
     tmem_st16(s_addr + q4 * 16, pk);
   }
-  if (kTrackMax) *raw_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
   return (sum[0].x + sum[0].y) + (sum[1].x + sum[1].y);
 }
 
@@ -761,7 +751,7 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           m_ref = m_new;
           // P first (the S row's registers are free after it), then O *= alpha: both land
           // before this tile's P-ready, which the PV of the tile waits for
-          l = l * alpha + exp_pack_store<kBf16, kM, kC, false, false>(sr, valid, c, m_use, s_addr);
+          l = l * alpha + exp_pack_store<kBf16, kM, kC, false>(sr, valid, c, m_use, s_addr);
           if (__any_sync(0xffffffffu, rescale) && j > 0) {
 #pragma unroll 1
             for (int q4 = 0; q4 < 4; ++q4) {
@@ -855,6 +845,7 @@ struct Smem1 {
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[kSBufs], p_ready[kSBufs], s_free[kSBufs];   // per S buffer
   uint64_t o_done, o_free;
+  uint64_t pv_issued[2];                // [T & 1]: a phase per two tiles, PV(T)'s MMAs are in the tensor queue
   uint64_t drain[2];
   uint32_t tmem_base;
   WaitCtl wc;
@@ -922,6 +913,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     }
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.o_free, kBM / 32);
+    for (int b = 0; b < 2; ++b) mbar_init(&sm.pv_issued[b], 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
@@ -998,9 +990,14 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (n >> 1) & 1, abort));
       for (int j = 0; ok && j < I.n_tiles; ++j) {
         const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj % kSBufs;
-        // K(T) landed, and S buffer sb is free: PV(T - 3) read its P
+        // K(T) landed, S buffer sb is free (PV(T - 3) read its P), and PV(T - 2) has been
+        // issued: the tensor queue then alternates PV(T - 2), QK(T), PV(T - 1), ... rather
+        // than holding QKs issued far ahead in front of the PV a softmax is waiting on.
+        // (PV(T - 1) may be issued too by then, so the token alternates between two
+        // barriers: a phase parity on one barrier could not tell T - 2 from T.)
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s], u & 1, abort) &&
-                                         (Tj < kSBufs || mbar_wait(&sm.s_free[sb], (Tj / kSBufs - 1) & 1, abort)));
+                                         (Tj < kSBufs || mbar_wait(&sm.s_free[sb], (Tj / kSBufs - 1) & 1, abort)) &&
+                                         (Tj < 2 || mbar_wait(&sm.pv_issued[Tj & 1], ((Tj - 2) >> 1) & 1, abort)));
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
@@ -1059,6 +1056,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           for (int kk = 0; kk < kBN / 16; ++kk)
             mma_ts(tmem + 384u, tmem + sb * 128u + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
                    (j > 0 || kk > 0) ? 1u : 0u);
+          mbar_arrive(&sm.pv_issued[Tj & 1]);
           mma_commit(&sm.s_free[sb]);
           mma_commit(&sm.v_empty[s]);
           if (j + 1 == I.n_tiles) mma_commit(&sm.o_done);
@@ -1108,23 +1106,22 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 #pragma unroll
           for (int q4 = 0; q4 < kC; ++q4) reg_fence32(sr + q4 * 32);
           // After the first tile, P is computed at once against the current reference
-          // max while the tile's max is found in the same pass; only if that max grew by
-          // more than the threshold (rare) is the tile redone against the new max, so
-          // the result is what the max-first order gives.
-          float m_tile;
+          // max.  Every p of the row is at most the row's sum of p, so a sum of at most
+          // 2^threshold shows that the tile's max did not grow by more than the threshold
+          // and P stands (the common case, which needs no max pass).  Otherwise (rare)
+          // the tile's max is found and the tile redone against it where it grew by more
+          // than the threshold: the same rescale decisions, and so the same result, as
+          // testing the tile's max itself.
           float lsum = 0.f;
           if (j > 0) {
-            float raw;
-            lsum = exp_pack_store<kBf16, kM, kC, true>(sr, valid, c, m_ref, s_addr, &raw);
-            m_tile = raw * c;
-          } else {
-            m_tile = row_max<kM, kC>(sr, valid) * c;
+            lsum = exp_pack_store<kBf16, kM, kC>(sr, valid, c, m_ref, s_addr);
+            if (!__any_sync(0xffffffffu, !(lsum <= kRescaleSum))) {   // (a NaN sum takes the slow path)
+              l += lsum;
+              return;
+            }
           }
-          bool rescale = m_tile > m_ref + kRescaleThreshold;
-          if (j > 0 && !__any_sync(0xffffffffu, rescale)) {
-            l += lsum;
-            return;
-          }
+          const float m_tile = row_max<kM, kC>(sr, valid) * c;
+          const bool rescale = m_tile > m_ref + kRescaleThreshold;
           const float m_new = rescale ? m_tile : m_ref;
           const float m_use = m_new == -INFINITY ? 0.f : m_new;
           if (j > 0) {
