@@ -204,12 +204,6 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle, sm_100 descriptor version.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
 // Instruction descriptor, kind::f16: fp32 accumulate, A/B 16-bit (fmt 0 fp16, 1 bf16),
 // A K-major, B K-major or MN-major, M = 128, N = 128.
 __host__ __device__ constexpr uint32_t idesc_f16(uint32_t fmt, uint32_t b_mn_major) {
@@ -217,19 +211,42 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t fmt, uint32_t b_mn_maj
          ((uint32_t)(kBM >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// Shared-memory matrix descriptor (128-byte swizzle, sm_100 descriptor version) as its
+// two 32-bit words: start address >> 4 in bits 0-13, leading-byte offset >> 4 in 16-29,
+// stride-byte offset >> 4 in 32-45, bit 46 set, layout 2 (128-byte swizzle) in 61-63.
+// The K steps of one MMA sequence differ only in the start address, so a sequence builds
+// the words once and adds each step's offset >> 4 to the low word: one 32-bit add per
+// step instead of rebuilding the 64-bit descriptor.  The address field is
+// (addr >> 4) & 0x3FFF; shared addresses are below 227 KB (< 14,528 in that unit) and a
+// step offset is at most 16,480 bytes (1,030), so the add never carries out of the field.
+struct SDesc {
+  uint32_t lo, hi;
+};
+__device__ __forceinline__ SDesc sdesc2(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return {((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16),
+          ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29)};
+}
+// kind::f16 MMA, A and B from shared memory: descriptors a and b advanced by a_off /
+// b_off bytes.
+__device__ __forceinline__ void mma_ss2(uint32_t d, SDesc a, uint32_t a_off, SDesc b, uint32_t b_off,
+                                        uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d),
+      "r"(a.lo + (a_off >> 4)), "r"(a.hi), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(acc)
       : "memory");
 }
-
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+// kind::f16 MMA, A from TMEM, B from shared memory advanced by b_off bytes.
+__device__ __forceinline__ void mma_ts2(uint32_t d, uint32_t a_tmem, SDesc b, uint32_t b_off, uint32_t idesc,
+                                        uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "r"(b.lo + (b_off >> 4)), "r"(b.hi), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -278,8 +295,8 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 
 // Per-warpgroup register split (all four warps of a warpgroup execute it): the pair
 // kernel launches 384 threads x 168 registers = 64,512; warps 0-3 (TMA producers and MMA
-// issuers) give theirs down to 80 and the two softmax warpgroups take 208 each:
-// 128 x 80 + 256 x 208 = 63,488, within the launch's total, so every increase is served.  The
+// issuers) give theirs down to 88 and the two softmax warpgroups take 208 each:
+// 128 x 88 + 256 x 208 = 64,512, the launch's total, so every increase is served.  The
 // launcher checks that the compiled kernel does launch with 168 registers per thread
 // (an increase beyond the launch's total would never be served).
 template <uint32_t kRegs> __device__ __forceinline__ void regs_dec() {
@@ -288,7 +305,7 @@ template <uint32_t kRegs> __device__ __forceinline__ void regs_dec() {
 template <uint32_t kRegs> __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
-constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 80, kRegsSoftmax = 208;
+constexpr uint32_t kRegsLaunch = 168, kRegsCtl = 88, kRegsSoftmax = 208;
 static_assert(128 * kRegsCtl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split above the launch's total");
 
 __device__ __forceinline__ float ex2(float x) {
@@ -544,28 +561,26 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // for those columns only.
     auto trimmed = [&](int rem) { return !p.causal && rem < kBN; };
     auto issue_qk = [&](int s, int rem) {
-      const uint32_t qa = smem_u32(sm.q[t]), ka = smem_u32(sm.k[s]);
+      const SDesc qd = sdesc2(smem_u32(sm.q[t]), 16, 1024), kd = sdesc2(smem_u32(sm.k[s]), 16, 1024);
       const uint32_t idesc =
           trimmed(rem) ? (kIdQK & ~(0x3Fu << 17)) | ((uint32_t)(((rem + 31) / 32) * 32 >> 3) << 17) : kIdQK;
 #pragma unroll
       for (int kk = 0; kk < kD / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-        mma_ss(tmem + s_col, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), idesc, kk > 0);
+        mma_ss2(tmem + s_col, qd, off, kd, off, idesc, kk > 0);
       }
     };
     auto pv_steps = [&](int rem) { return trimmed(rem) ? (rem + 15) / 16 : kBN / 16; };
     auto issue_pv = [&](int s, int j, int steps) {
-      const uint32_t va = smem_u32(sm.v[s]);
+      const SDesc vd = sdesc2(smem_u32(sm.v[s]), kBoxBytes, 1024);
       if (steps == kBN / 16) {
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts2(tmem + o_col, tmem + s_col + kk * 8, vd, kk * 16 * 128, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
       } else {
 #pragma unroll 1
         for (int kk = 0; kk < steps; ++kk)
-          mma_ts(tmem + o_col, tmem + s_col + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts2(tmem + o_col, tmem + s_col + kk * 8, vd, kk * 16 * 128, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
       }
     };
     int T = 0, n_items_done = 0;
@@ -1001,11 +1016,11 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t qa = smem_u32(sm.q[qb]), ka = smem_u32(sm.k[s]);
+          const SDesc qd = sdesc2(smem_u32(sm.q[qb]), 16, 1024), kd = sdesc2(smem_u32(sm.k[s]), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-            mma_ss(tmem + sb * 128u, sdesc(qa + off, 16, 1024), sdesc(ka + off, 16, 1024), kIdQK, kk > 0);
+            mma_ss2(tmem + sb * 128u, qd, off, kd, off, kIdQK, kk > 0);
           }
           mma_commit(&sm.s_full[sb]);
           mma_commit(&sm.k_empty[s]);
@@ -1051,11 +1066,10 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t va = smem_u32(sm.v[s]);
+          const SDesc vd = sdesc2(smem_u32(sm.v[s]), kBoxBytes, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tmem + 384u, tmem + sb * 128u + kk * 8, sdesc(va + kk * 16 * 128, kBoxBytes, 1024), kIdPV,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts2(tmem + 384u, tmem + sb * 128u + kk * 8, vd, kk * 16 * 128, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
           mbar_arrive(&sm.pv_issued[Tj & 1]);
           mma_commit(&sm.s_free[sb]);
           mma_commit(&sm.v_empty[s]);
