@@ -860,7 +860,7 @@ struct Smem1 {
   uint64_t v_full[kStages], v_empty[kStages];
   uint64_t s_full[kSBufs], p_ready[kSBufs], s_free[kSBufs];   // per S buffer
   uint64_t o_done, o_free;
-  uint64_t pv_issued[2];                // [T & 1]: a phase per two tiles, PV(T)'s MMAs are in the tensor queue
+  uint64_t pv_issued[2];                // [T & 1]: a phase per two tiles, PV(T)'s MMAs are being queued
   uint64_t drain[2];
   uint32_t tmem_base;
   WaitCtl wc;
@@ -1005,10 +1005,12 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (n >> 1) & 1, abort));
       for (int j = 0; ok && j < I.n_tiles; ++j) {
         const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj % kSBufs;
-        // K(T) landed, S buffer sb is free (PV(T - 3) read its P), and PV(T - 2) has been
-        // issued: the tensor queue then alternates PV(T - 2), QK(T), PV(T - 1), ... rather
+        // K(T) landed, S buffer sb is free (PV(T - 3) read its P), and PV(T - 2) is being
+        // issued (the PV issuer signals once half its MMAs are queued, so that this
+        // thread's wake-up overlaps the rest and the tensor pipe does not drain between
+        // the two): the queue then alternates PV(T - 2), QK(T), PV(T - 1), ... rather
         // than holding QKs issued far ahead in front of the PV a softmax is waiting on.
-        // (PV(T - 1) may be issued too by then, so the token alternates between two
+        // (PV(T - 1) may be signalled too by then, so the token alternates between two
         // barriers: a phase parity on one barrier could not tell T - 2 from T.)
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.k_full[s], u & 1, abort) &&
                                          (Tj < kSBufs || mbar_wait(&sm.s_free[sb], (Tj / kSBufs - 1) & 1, abort)) &&
@@ -1068,9 +1070,10 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (lane == 0) {
           const SDesc vd = sdesc2(smem_u32(sm.v[s]), kBoxBytes, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
+          for (int kk = 0; kk < kBN / 16; ++kk) {
             mma_ts2(tmem + 384u, tmem + sb * 128u + kk * 8, vd, kk * 16 * 128, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-          mbar_arrive(&sm.pv_issued[Tj & 1]);
+            if (kk == 3) mbar_arrive(&sm.pv_issued[Tj & 1]);
+          }
           mma_commit(&sm.s_free[sb]);
           mma_commit(&sm.v_empty[s]);
           if (j + 1 == I.n_tiles) mma_commit(&sm.o_done);
