@@ -119,3 +119,39 @@ def test_merge_rows_without_keys():
         bound = merge_lse_error_bound(la64, lb64, zero, zero)
     bound = np.where(np.isfinite(la64) & np.isfinite(lb64), bound, 2.0 ** -20 + 2.0 ** -23 * np.abs(ref_l))
     assert np.all(np.abs(lo.double().cpu().numpy()[fin] - ref_l[fin]) <= bound[fin])
+
+
+@pytest.mark.parametrize("case", ["vector_ragged", "odd_head_dim", "unaligned"])
+def test_merge_paths_match_oracle(case):
+    """A ragged row count, a row size that is not a multiple of 16 bytes and buffers off
+    a 16-byte boundary all give the oracle's merge, and rows without keys give 0 and
+    -inf."""
+    rows, D = (1001, 128) if case != "odd_head_dim" else (257, 72)
+    g = torch.Generator(device="cuda").manual_seed(31)
+    pad = 1 if case == "unaligned" else 0
+    base_a = torch.randn(rows * D + pad, device="cuda", generator=g).bfloat16()
+    base_b = torch.randn(rows * D + pad, device="cuda", generator=g).bfloat16()
+    oa, ob = base_a[pad:].view(rows, D), base_b[pad:].view(rows, D)
+    la = torch.randn(rows, device="cuda", generator=g) * 4
+    lb = torch.randn(rows, device="cuda", generator=g) * 4
+    la[5] = float("-inf")
+    la[7] = lb[7] = float("-inf")
+    out_base = torch.full((rows * D + pad,), float("nan"), device="cuda").bfloat16()
+    out = out_base[pad:].view(rows, D)
+    lo = torch.empty_like(la)
+    kvc.kvc_merge(torch.bfloat16, rows, D, oa, la, ob, lb, out, lo)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.merge_lse(to64(oa), la.double().cpu().numpy(), to64(ob), lb.double().cpu().numpy())
+    got = to64(out)
+    assert np.all(np.isfinite(got))
+    # the fp32 combination (weights from expf / logf / a division: a few ulp each) then
+    # one bf16 rounding (unit roundoff 2^-8): |err| <= 2^-8 |o| + 2^-19 (|wa oa| + |wb ob|)
+    la64, lb64 = la.double().cpu().numpy(), lb.double().cpu().numpy()
+    safe = np.where(np.isfinite(ref_l), ref_l, 0.0)
+    wa = np.where(np.isfinite(la64), np.exp(la64 - safe), 0.0)[:, None]
+    wb = np.where(np.isfinite(lb64), np.exp(lb64 - safe), 0.0)[:, None]
+    mag = np.abs(wa * to64(oa)) + np.abs(wb * to64(ob))
+    assert np.all(np.abs(got - ref_o) <= 2.0 ** -8 * np.abs(ref_o) + 2.0 ** -19 * mag)
+    assert torch.all(out[7] == 0) and torch.isneginf(lo[7])
+    fin = np.isfinite(ref_l)
+    assert np.allclose(lo.double().cpu().numpy()[fin], ref_l[fin], rtol=1e-6, atol=1e-5)
