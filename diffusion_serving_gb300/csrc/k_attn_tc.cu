@@ -843,21 +843,22 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 // spans three tiles and the softmax warps, not the MMA issue, set the pace.  O is read
 // by the epilogue before the next item's first PV (o_free): one bubble per item, which
 // is small on the long rows this kernel is for.
-// Warps (256 threads): 0 TMA producer of Q (double-buffered per item) and K, 3 TMA
-// producer of V (two-stage rings each), 1 QK issuer and TMEM owner, 2 PV issuer (and
+// Warps (256 threads): 0 TMA producer of Q (one buffer, reloaded once the item's last
+// QK is done) and K (three-stage ring), 3 TMA producer of V (two-stage ring), 1 QK issuer and TMEM owner, 2 PV issuer (and
 // V-tail zeroing), 4-7 softmax and epilogue of the tile's 128 rows (warp & 3 = TMEM lane
 // quadrant).
 constexpr int kSBufs = 3;
+constexpr int kKStages1 = 3, kVStages1 = 2;   // K and V ring depths
 constexpr int kThreads1 = 256;
 
 struct Smem1 {
-  uint8_t q[2][kTileBytes];             // Q tile per item, double-buffered
-  uint8_t k[kStages][kTileBytes];
-  uint8_t v[kStages][kTileBytes];
+  uint8_t q[kTileBytes];                // Q tile of the item
+  uint8_t k[kKStages1][kTileBytes];
+  uint8_t v[kVStages1][kTileBytes];
   uint8_t o_stage[4][2][kStageBytes];   // output staging per softmax warp (64-byte swizzle)
-  uint64_t q_full[2], q_free[2];
-  uint64_t k_full[kStages], k_empty[kStages];
-  uint64_t v_full[kStages], v_empty[kStages];
+  uint64_t q_full, q_free;
+  uint64_t k_full[kKStages1], k_empty[kKStages1];
+  uint64_t v_full[kVStages1], v_empty[kVStages1];
   uint64_t s_full[kSBufs], p_ready[kSBufs], s_free[kSBufs];   // per S buffer
   uint64_t o_done, o_free;
   uint64_t pv_issued[2];                // [T & 1]: a phase per two tiles, PV(T)'s MMAs are being queued
@@ -916,11 +917,9 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
   volatile WaitCtl* abort = &sm.wc;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.q_full[b], 1);
-      mbar_init(&sm.q_free[b], 1);
-      mbar_init(&sm.drain[b], 1);
-    }
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_free, 1);
+    for (int b = 0; b < 2; ++b) mbar_init(&sm.drain[b], 1);
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(&sm.s_full[b], 1);
       mbar_init(&sm.p_ready[b], kBM / 32);   // one arrival per softmax warp
@@ -929,9 +928,11 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.o_free, kBM / 32);
     for (int b = 0; b < 2; ++b) mbar_init(&sm.pv_issued[b], 1);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages1; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages1; ++s) {
       mbar_init(&sm.v_full[s], 1);
       mbar_init(&sm.v_empty[s], 1);
     }
@@ -952,6 +953,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     // (two threads, so that a K load never queues behind a V load waiting for a PV)
     if (lane == 0) {
       const bool kq = warp == 0;
+      const int stages = kq ? kKStages1 : kVStages1;
       int T = 0, n = 0;
       RowCache rc;
       int issued = 0, q_issued = 0;
@@ -960,20 +962,19 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         Item I;
         if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
         if (kq) {
-          const int qb = n & 1;
-          if (n >= 2 && !mbar_wait(&sm.q_free[qb], ((n >> 1) - 1) & 1, abort)) break;   // item n - 2's last QK
-          mbar_expect_tx(&sm.q_full[qb], kTileBytes);
+          if (n >= 1 && !mbar_wait(&sm.q_free, (n - 1) & 1, abort)) break;   // item n - 1's last QK
+          mbar_expect_tx(&sm.q_full, kTileBytes);
           for (int half = 0; half < 2; ++half)
-            tma_load_4d(&tm_q, &sm.q_full[qb], sm.q[qb] + half * kBoxBytes, half * 64, I.h, I.row_a, I.b);
+            tma_load_4d(&tm_q, &sm.q_full, sm.q + half * kBoxBytes, half * 64, I.h, I.row_a, I.b);
           q_issued = n + 1;
         }
         const CUtensorMap* tm = kq ? &tm_k : &tm_v;
         for (int j = 0; j < I.n_tiles; ++j) {
-          const int Tj = T + j, s = Tj % kStages, u = Tj / kStages;
+          const int Tj = T + j, s = Tj % stages, u = Tj / stages;
           uint64_t* empty = kq ? &sm.k_empty[s] : &sm.v_empty[s];
           uint64_t* full = kq ? &sm.k_full[s] : &sm.v_full[s];
           uint8_t* dst = kq ? sm.k[s] : sm.v[s];
-          if (Tj >= kStages && !mbar_wait(empty, (u - 1) & 1, abort)) {
+          if (Tj >= stages && !mbar_wait(empty, (u - 1) & 1, abort)) {
             ok = false;
             break;
           }
@@ -987,9 +988,9 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       }
       if (abort->abort) {
         // drain: every load this thread issued lands before the CTA's shared memory is released
-        for (int m = max(0, q_issued - 2); m < q_issued; ++m) mbar_wait(&sm.q_full[m & 1], (m >> 1) & 1, abort, false);
-        for (int j = max(0, issued - kStages); j < issued; ++j)
-          mbar_wait(kq ? &sm.k_full[j % kStages] : &sm.v_full[j % kStages], (j / kStages) & 1, abort, false);
+        if (q_issued > 0) mbar_wait(&sm.q_full, (q_issued - 1) & 1, abort, false);
+        for (int j = max(0, issued - stages); j < issued; ++j)
+          mbar_wait(kq ? &sm.k_full[j % stages] : &sm.v_full[j % stages], (j / stages) & 1, abort, false);
       }
     }
   } else if (warp == 1) {
@@ -1001,10 +1002,9 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       Item I;
       if (!item_geom1(item, qtiles, p, meta, rc, &I)) continue;
-      const int qb = n & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full[qb], (n >> 1) & 1, abort));
+      ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, n & 1, abort));
       for (int j = 0; ok && j < I.n_tiles; ++j) {
-        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj % kSBufs;
+        const int Tj = T + j, s = Tj % kKStages1, u = Tj / kKStages1, sb = Tj % kSBufs;
         // K(T) landed, S buffer sb is free (PV(T - 3) read its P), and PV(T - 2) is being
         // issued (the PV issuer signals once half its MMAs are queued, so that this
         // thread's wake-up overlaps the rest and the tensor pipe does not drain between
@@ -1018,7 +1018,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         if (!ok) break;
         tc_fence_after();
         if (lane == 0) {
-          const SDesc qd = sdesc2(smem_u32(sm.q[qb]), 16, 1024), kd = sdesc2(smem_u32(sm.k[s]), 16, 1024);
+          const SDesc qd = sdesc2(smem_u32(sm.q), 16, 1024), kd = sdesc2(smem_u32(sm.k[s]), 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
@@ -1026,7 +1026,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
           }
           mma_commit(&sm.s_full[sb]);
           mma_commit(&sm.k_empty[s]);
-          if (j + 1 == I.n_tiles) mma_commit(&sm.q_free[qb]);
+          if (j + 1 == I.n_tiles) mma_commit(&sm.q_free);
         }
         __syncwarp();
       }
@@ -1050,7 +1050,7 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       // O is free once the epilogue of item n - 1 has read it
       ok = __all_sync(0xffffffffu, n < 1 || mbar_wait(&sm.o_free, (n - 1) & 1, abort));
       for (int j = 0; ok && j < I.n_tiles; ++j) {
-        const int Tj = T + j, s = Tj % kStages, u = Tj / kStages, sb = Tj % kSBufs;
+        const int Tj = T + j, s = Tj % kVStages1, u = Tj / kVStages1, sb = Tj % kSBufs;
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.v_full[s], u & 1, abort));
         if (!ok) break;
         const int rem = I.kv_end - j * kBN;
