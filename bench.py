@@ -286,6 +286,28 @@ def decode_bench(kvc, peaks, per_graph=64, replays=5):
     res["step_append_attend"] = {"kv_len": f"{wl.DECODE_PROMPT + 1}..{wl.DECODE_PROMPT + replays * per_graph}",
                                  "us": round(t * 1e6, 3), "tokens_per_s": round(1.0 / t, 1),
                                  "timing": f"graph of {per_graph} steps x {replays} replays"}
+    # the whole step in one launch (kvc_append_attend_decode)
+    c.reset()
+    c.append(kp, kp)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(graph, stream=side):
+        for r in range(per_graph):
+            c.append_attend(k1, k1, q, out, stream=side)
+    graph.replay()
+    c.reset()
+    c.append(kp, kp)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(replays):
+        graph.replay()
+    b.record()
+    b.synchronize()
+    t = a.elapsed_time(b) * 1e-3 / (replays * per_graph)
+    res["step_fused_append_attend"] = {"kv_len": f"{wl.DECODE_PROMPT + 1}..{wl.DECODE_PROMPT + replays * per_graph}",
+                                       "us": round(t * 1e6, 3), "tokens_per_s": round(1.0 / t, 1),
+                                       "timing": f"graph of {per_graph} steps x {replays} replays"}
     for c in caches:
         assert c.get_error() == 0
     return res
@@ -434,7 +456,7 @@ def tiny_bench(kvc, reps=20):
 def decode_schedule_bench(kvc, peaks, reps=5):
     """The active-prefix workload as the pages run it (fp16, H 32 / Hkv 8, D 128, a
     32768-slot store): prefill of 234 tokens (append, causal attend of the 234 queries),
-    then 512 decode steps (append the token's K/V in one launch, attend), kv_len
+    then 512 decode steps (append the token's K/V and attend, one launch per step), kv_len
     235..746.  The 512 steps are one captured graph; tokens/s = 512 / their time."""
     w = wl.DECODE
     T, N = wl.DECODE_PROMPT, wl.DECODE_STEPS
@@ -456,14 +478,12 @@ def decode_schedule_bench(kvc, peaks, reps=5):
     with torch.cuda.stream(side):
         prefill()
         for _ in range(3):
-            c.append(k1, k1, stream=side)
-            c.attend(q1, o1, stream=side)
+            c.append_attend(k1, k1, q1, o1, stream=side)
         side.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=side):
             for _ in range(N):
-                c.append(k1, k1, stream=side)
-                c.attend(q1, o1, stream=side)
+                c.append_attend(k1, k1, q1, o1, stream=side)
         a, b, m = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         t_pre = t_dec = 0.0
         for _ in range(reps + 1):
@@ -483,7 +503,7 @@ def decode_schedule_bench(kvc, peaks, reps=5):
             "decode_ms": round(t_dec * 1e3, 4), "tokens_per_s": round(N / t_dec, 1),
             "us_per_step": round(t_dec / N * 1e6, 3),
             "kv_GB/s": round(kv_bytes / t_dec / 1e9, 1), "kv_frac": round(kv_bytes / t_dec / 1e9 / peaks["hbm"], 4),
-            "timing": f"prefill eager + {N} steps (append + attend) as one graph, {reps} runs; "
+            "timing": f"prefill eager + {N} steps (fused append + attend) as one graph, {reps} runs; "
                       f"kv_len {T + 1}..{T + N}, latency-bound"}
 
 

@@ -163,6 +163,8 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, const __nv_bfloat1
 }
 __device__ __forceinline__ void store_out(__half* p, float x) { *p = __float2half_rn(x); }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+__device__ __forceinline__ float load_f(const __half* p) { return __half2float(*p); }
+__device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -179,11 +181,12 @@ __host__ __device__ constexpr uint32_t stage_bytes() { return 2u * (D / 64) * kH
 template <int D>
 __host__ __device__ constexpr size_t dyn_smem_bytes() { return (size_t)kStages * stage_bytes<D>() + 1024; }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool kApp>
 __global__ void __launch_bounds__(kThreads, 1)
 k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v, const T* __restrict__ q,
          T* __restrict__ out, int32_t* __restrict__ meta, float* __restrict__ ws, kvc_geom g, float scale_log2,
-         float* __restrict__ lse, int fixed_tiles, uint64_t stall_ns) {
+         float* __restrict__ lse, int fixed_tiles, uint64_t stall_ns, const T* __restrict__ k_new,
+         const T* __restrict__ v_new, T* __restrict__ k_store, T* __restrict__ v_store) {
   constexpr int HB = D / 64;         // 64-dim boxes per K (or V) tile
   constexpr int NT = D / 8;          // n-tiles of 8 dims in O
   constexpr uint32_t SB = stage_bytes<D>();
@@ -194,7 +197,9 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   float (*s_acc)[G][D] = reinterpret_cast<float (*)[G][D]>(dsm);
   __shared__ float s_ml[kWarps][G][2];
   __shared__ float s_inv[G], s_max[G];
-  __shared__ int s_last;
+  __shared__ int s_last, s_upd;
+  __shared__ float s_snew[G], s_pnew[G];   // append: the new key's score (exp2 domain) and weight
+  __shared__ float s_vnew[D];               // append: the new token's value row
   __shared__ WaitCtl s_wc;
   __shared__ int s_tile[kStages];    // tile index held by each stage, -1: no more tiles
 
@@ -225,8 +230,73 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 
   kvc_pdl_wait();
   kvc_pdl_release();
+  // Append-then-attend (k_new set, LINEAR): the row's keys are its `filled` stored slots
+  // plus the new token, which this launch also writes to slot `filled`; every block reads
+  // its row's length, then the last block to arrive advances every row's meta (reserved
+  // chunks, base, filled, kv_len: what kvc_append does) and clears the counter.
+  constexpr bool app = kApp;
+  constexpr int kNew = kApp ? D / 32 : 1;
+  T nk[kNew], nv[kNew], nq[G][kNew];   // append, warp 0: this lane's dims of the new token and queries
   int row0 = 0, len = 0;
-  if (!kvc_row_range(g, b, &row0, &len, meta + KVC_META_ERR)) return;
+  bool row_ok;
+  if (app) {
+    len = meta[kvc_meta_row(b) + KVC_ROW_FILLED];
+    row_ok = len >= 0 && (int64_t)len + 1 <= g.cap;
+    if (!row_ok && threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(meta + KVC_META_ERR, KVC_DEV_OVERFLOW);
+    __syncthreads();   // every thread's read of the row's length precedes the arrival below
+    if (warp == 0) {
+      // Warp 0 alone (the producer warp goes on to issue the first loads, whose latency
+      // covers this): arrive, advance every row if this block is the last to arrive, and
+      // (block 0 of the pair) store the new token's K and V rows of this kv head at slot
+      // `len`, which no block of this launch reads (its key comes from k_new / v_new).
+      constexpr unsigned kAll = 0xffffffffu;
+      int upd = 0;
+      if (lane == 0) {
+        int prev;
+        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(meta + KVC_META_ARRIVE) : "memory");
+        upd = prev == (int)(gridDim.x * gridDim.y * gridDim.z) - 1;
+      }
+      upd = __shfl_sync(kAll, upd, 0);
+      __syncwarp(kAll);   // orders lane 0's acquire before the other lanes' meta writes
+      if (upd) {
+        for (int bb = lane; bb < g.B; bb += 32) {
+          int32_t* m = meta + kvc_meta_row(bb);
+          const int f = m[KVC_ROW_FILLED];
+          if (f >= 0 && (int64_t)f + 1 <= g.cap) {
+            m[KVC_ROW_CHUNKS] += 1;
+            m[KVC_ROW_BASE] = f;
+            m[KVC_ROW_FILLED] = f + 1;
+            m[KVC_ROW_KVLEN] = f + 1;
+          }
+        }
+        __syncwarp(kAll);
+        if (lane == 0) meta[KVC_META_ARRIVE] = 0;
+      }
+      if (row_ok) {   // the new token's key, value and the heads' queries, in flight during the stream
+        const int64_t kv_off = ((int64_t)b * g.Hkv + kvh) * D;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          nk[i] = k_new[kv_off + lane + 32 * i];
+          nv[i] = v_new[kv_off + lane + 32 * i];
+#pragma unroll
+          for (int gg = 0; gg < G; ++gg) nq[gg][i] = q[((int64_t)b * g.H + kvh * G + gg) * D + lane + 32 * i];
+        }
+      }
+      constexpr int kRowVecs = D * (int)sizeof(T) / 16;
+      if (row_ok && split == 0) {
+        for (int i = lane; i < 2 * kRowVecs; i += 32) {
+          const int t = i / kRowVecs, c = i - t * kRowVecs;
+          const uint4* src = reinterpret_cast<const uint4*>((t ? v_new : k_new) + ((int64_t)b * g.Hkv + kvh) * D) + c;
+          uint4* dst =
+              reinterpret_cast<uint4*>((t ? v_store : k_store) + (((int64_t)b * g.cap + len) * g.Hkv + kvh) * D) + c;
+          *dst = __ldg(src);
+        }
+      }
+    }
+  } else {
+    row_ok = kvc_row_range(g, b, &row0, &len, meta + KVC_META_ERR);
+  }
+  if (!row_ok) return;
 
   // Tiles of kTile slots of this row: block `split` takes tiles split, split + nsplit, ...
   // for its first kStages tiles, then claims tiles kStages * nsplit, ... one at a time
@@ -394,6 +464,19 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
   }
+  if (app && warp == 0) {   // the new key's score per head (exp2 domain) and its value row
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) acc = fmaf(load_f(&nq[gg][i]), load_f(&nk[i]), acc);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) s_snew[gg] = acc * scale_log2;
+    }
+#pragma unroll
+    for (int i = 0; i < D / 32; ++i) s_vnew[lane + 32 * i] = load_f(&nv[i]);
+  }
   __syncthreads();                                  // every warp (and every load) is done with the ring
   if (warp < kWarps && hq < G) {
 #pragma unroll
@@ -419,6 +502,12 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const float mw = s_ml[w][gg][0];
         if (mw != -INFINITY) L = fmaf(ex2(mw - M), s_ml[w][gg][1], L);
       }
+      if (app) {   // the new key joins with weight 2^(s - M)
+        const float sn = s_snew[gg], M2 = fmaxf(M, sn);
+        L = (M == -INFINITY ? 0.f : L * ex2(M - M2)) + ex2(sn - M2);
+        M = M2;
+        s_pnew[gg] = ex2(sn - M);
+      }
       s_max[gg] = M;
       s_inv[gg] = 1.f / L;
       if (lse != nullptr) lse[(int64_t)b * g.H + kvh * G + gg] = (M + log2f(L)) * 0.6931471805599453f;
@@ -433,6 +522,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
         const float mw = s_ml[w][gg][0];
         if (mw != -INFINITY) a = fmaf(ex2(mw - M), s_acc[w][gg][d], a);
       }
+      if (app) a = fmaf(s_pnew[gg], s_vnew[d], a);
       store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, a * s_inv[gg]);
     }
     return;
@@ -502,6 +592,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     for (int s = lane; s < used; s += 32) M = fmaxf(M, sw[gg * used + s]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (app) M = fmaxf(M, s_snew[gg]);
     float L = 0.f;
     for (int s = lane; s < used; s += 32) {
       const float ms = sw[gg * used + s];
@@ -512,6 +603,10 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     if (lane == 0) {
+      if (app) {   // the new key joins with weight 2^(s - M)
+        s_pnew[gg] = ex2(s_snew[gg] - M);
+        L += s_pnew[gg];
+      }
       s_inv[gg] = 1.f / L;
       if (lse != nullptr) lse[(int64_t)b * g.H + kvh * G + gg] = (M + log2f(L)) * 0.6931471805599453f;
     }
@@ -528,6 +623,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     for (int k = 0; k < kPre; ++k)
       if (k < used) o[k & 3] = fmaf(wrow[k], pre[i][k], o[k & 3]);
     for (int k = kPre; k < used; ++k) o[k & 3] = fmaf(wrow[k], __ldcg(ws_pair + (int64_t)k * G * D + e), o[k & 3]);
+    if (app) o[0] = fmaf(s_pnew[gg], s_vnew[d], o[0]);
     store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, ((o[0] + o[1]) + (o[2] + o[3])) * s_inv[gg]);
   }
   if (threadIdx.x == 0) {           // every block of the pair is past both counters
@@ -536,32 +632,51 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   }
 }
 
+// The new token of an append-then-attend decode ([B, 1, Hkv, D] each), or none.
+struct DecAppend {
+  const void* k = nullptr;
+  const void* v = nullptr;
+};
+
 template <typename T, int D, int G>
-cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare) {
+cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare,
+                      const DecAppend& ap) {
   constexpr size_t smem = dyn_smem_bytes<D>();
-  if (prepare) return cudaFuncSetAttribute(k_decode<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (prepare) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_decode<T, D, G, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_decode<T, D, G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  }
   const kvc_config& cfg = c->cfg;
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout, c->lens};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
-  return kvc_launch_pdl(k_decode<T, D, G>, grid, dim3(kThreads), smem, s, c->tm_dk, c->tm_dv, (const T*)q, (T*)out,
-                        c->meta, (float*)c->ws, g, c->scale * 1.4426950408889634f, lse, fixed,
-                        c->debug_stall_ns);
+  const float sl2 = c->scale * 1.4426950408889634f;
+  if (ap.k == nullptr)
+    return kvc_launch_pdl(k_decode<T, D, G, false>, grid, dim3(kThreads), smem, s, c->tm_dk, c->tm_dv, (const T*)q,
+                          (T*)out, c->meta, (float*)c->ws, g, sl2, lse, fixed, c->debug_stall_ns, (const T*)nullptr,
+                          (const T*)nullptr, (T*)c->k, (T*)c->v);
+  return kvc_launch_pdl(k_decode<T, D, G, true>, grid, dim3(kThreads), smem, s, c->tm_dk, c->tm_dv, (const T*)q,
+                        (T*)out, c->meta, (float*)c->ws, g, sl2, lse, fixed, c->debug_stall_ns, (const T*)ap.k,
+                        (const T*)ap.v, (T*)c->k, (T*)c->v);
 }
 
 template <typename T, int D>
-cudaError_t launch_d(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare) {
+cudaError_t launch_d(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare,
+                     const DecAppend& ap) {
   switch (c->cfg.heads / c->cfg.kv_heads) {
-    case 1: return launch_dg<T, D, 1>(c, q, out, lse, fixed, s, prepare);
-    case 2: return launch_dg<T, D, 2>(c, q, out, lse, fixed, s, prepare);
-    case 4: return launch_dg<T, D, 4>(c, q, out, lse, fixed, s, prepare);
-    default: return launch_dg<T, D, 8>(c, q, out, lse, fixed, s, prepare);
+    case 1: return launch_dg<T, D, 1>(c, q, out, lse, fixed, s, prepare, ap);
+    case 2: return launch_dg<T, D, 2>(c, q, out, lse, fixed, s, prepare, ap);
+    case 4: return launch_dg<T, D, 4>(c, q, out, lse, fixed, s, prepare, ap);
+    default: return launch_dg<T, D, 8>(c, q, out, lse, fixed, s, prepare, ap);
   }
 }
 
 template <typename T>
-cudaError_t launch_t(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare) {
-  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, lse, fixed, s, prepare)
-                               : launch_d<T, 128>(c, q, out, lse, fixed, s, prepare);
+cudaError_t launch_t(kvc_cache* c, const void* q, void* out, float* lse, int fixed, cudaStream_t s, bool prepare,
+                     const DecAppend& ap = DecAppend()) {
+  return c->cfg.head_dim == 64 ? launch_d<T, 64>(c, q, out, lse, fixed, s, prepare, ap)
+                               : launch_d<T, 128>(c, q, out, lse, fixed, s, prepare, ap);
 }
 
 // The decode kernels opt into their dynamic shared memory once per process and
@@ -616,6 +731,17 @@ cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse
   const int fixed = fixed_tiles ? 1 : 0;
   return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, lse, fixed, s, false)
                                  : launch_t<__nv_bfloat16>(c, q, out, lse, fixed, s, false);
+}
+
+cudaError_t kvc_launch_decode_append(kvc_cache* c, const void* k_new, const void* v_new, const void* q, void* out,
+                                     cudaStream_t s) {
+  const cudaError_t e = prepare_once(c);
+  if (e != cudaSuccess) return e;
+  DecAppend ap;
+  ap.k = k_new;
+  ap.v = v_new;
+  return c->cfg.dtype == KVC_F16 ? launch_t<__half>(c, q, out, nullptr, 0, s, false, ap)
+                                 : launch_t<__nv_bfloat16>(c, q, out, nullptr, 0, s, false, ap);
 }
 
 // ---------------------------------------------------------------------------

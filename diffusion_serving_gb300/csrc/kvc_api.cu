@@ -222,6 +222,14 @@ int kvc_append(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, voi
   return launched(kvc_launch_write(c, k, v, n_tokens, nullptr, s));
 }
 
+int kvc_append_attend_decode(kvc_cache* c, const void* k_new, const void* v_new, const void* q, void* out,
+                             void* stream) {
+  if (c == nullptr || !k_new || !v_new || !q || !out) return KVC_ERR_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(q) || !aligned16(out)) return KVC_ERR_ARG;
+  if (c->cfg.layout != KVC_LINEAR || c->dec_splits <= 0 || c->bound != nullptr) return KVC_ERR_UNSUPPORTED;
+  return launched(kvc_launch_decode_append(c, k_new, v_new, q, out, as_stream(stream)));
+}
+
 int kvc_write_rope(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, const int32_t* d_slots,
                    const float* d_rope, int32_t rope_positions, void* stream) {
   if (c == nullptr || !k || !v || !aligned16(k) || !aligned16(v) || n_tokens < 1) return KVC_ERR_ARG;

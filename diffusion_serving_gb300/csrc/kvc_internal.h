@@ -9,6 +9,7 @@
 
 // ---- meta block layout (int32 words; documented in kvc.h) -------------------
 #define KVC_META_ERR 0
+#define KVC_META_ARRIVE 1   // blocks of an append-then-attend decode launch that have read their lengths
 #define KVC_META_ROW0 4
 #define KVC_ROW_CHUNKS 0   // chunks reserved so far
 #define KVC_ROW_BASE 1     // first slot of the reserved chunk
@@ -134,6 +135,8 @@ cudaError_t kvc_launch_append(kvc_cache* c, const void* k, const void* v, int n,
 cudaError_t kvc_launch_attn_simt(kvc_cache* c, const void* q, void* out, int n_q, bool causal, float* lse,
                                  cudaStream_t s);
 cudaError_t kvc_launch_decode(kvc_cache* c, const void* q, void* out, float* lse, bool fixed_tiles, cudaStream_t s);
+cudaError_t kvc_launch_decode_append(kvc_cache* c, const void* k_new, const void* v_new, const void* q, void* out,
+                                     cudaStream_t s);
 cudaError_t kvc_prepare_decode(kvc_cache* c);
 bool kvc_decode_supported(const kvc_config& cfg);
 int kvc_internal_check_config(const kvc_config* cfg, int* cap);

@@ -59,6 +59,7 @@ def _load():
         "kvc_write": (ctypes.c_int, [P, P, P, I32, P, P]),
         "kvc_write_rope": (ctypes.c_int, [P, P, P, I32, P, P, I32, P]),
         "kvc_append": (ctypes.c_int, [P, P, P, I32, P]),
+        "kvc_append_attend_decode": (ctypes.c_int, [P, P, P, P, P, P]),
         "kvc_set_lengths": (ctypes.c_int, [P, P, P, P]),
         "kvc_attend": (ctypes.c_int, [P, P, P, I32, U32, P]),
         "kvc_attend_lse": (ctypes.c_int, [P, P, P, P, I32, U32, P]),
@@ -154,6 +155,11 @@ def kvc_write(h: int, k, v, n_tokens: int, slots=None, stream=None) -> None:
 
 def kvc_append(h: int, k, v, n_tokens: int, stream=None) -> None:
     _check(_lib.kvc_append(h, _ptr(k), _ptr(v), n_tokens, _stream(stream)), "kvc_append")
+
+
+def kvc_append_attend_decode(h: int, k_new, v_new, q, out, stream=None) -> None:
+    _check(_lib.kvc_append_attend_decode(h, _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out), _stream(stream)),
+           "kvc_append_attend_decode")
 
 
 def kvc_write_rope(h: int, k, v, n_tokens: int, rope, rope_positions: int, slots=None, stream=None) -> None:
@@ -340,6 +346,18 @@ class KVCache:
         """Reserve k.shape[1] slots after those filled (LINEAR) and write k, v there."""
         self._check_kv(k, v)
         kvc_append(self.handle, k, v, k.shape[1], stream)
+
+    def append_attend(self, k, v, q, out=None, stream=None):
+        """One decode step in one launch: append one token per row (k, v [B, 1, Hkv, D])
+        and attend q [B, 1, H, D] over the prefix with it (LINEAR, 16-bit)."""
+        self._check_kv(k, v)
+        if k.shape[1] != 1 or q.shape[1] != 1:
+            raise ValueError("kvc: append_attend takes one new token and one query per row")
+        if out is None:
+            out = torch.empty_like(q)
+        self._check_q(q, out)
+        kvc_append_attend_decode(self.handle, k, v, q, out, stream)
+        return out
 
     def write_rope(self, k, v, rope, slots=None, stream=None):
         """Write with K rotated by the (cos, sin) table ``rope`` [positions, D/2, 2] fp32."""

@@ -170,6 +170,22 @@ int kvc_write(kvc_cache* c, const void* k, const void* v, int32_t n_tokens,
  * capacity, KVC_ERR_ARG, KVC_ERR_CUDA. */
 int kvc_append(kvc_cache* c, const void* k, const void* v, int32_t n_tokens, void* stream);
 
+/* One decode step in one launch: append one token per row (k_new, v_new: device,
+ * [B, 1, Hkv, D], 16-byte aligned) and attend q (device [B, 1, H, D]) over every row's
+ * stored prefix plus that token, writing out (device [B, 1, H, D]).  The same result as
+ * kvc_append(c, k_new, v_new, 1) followed by kvc_attend(c, q, out, 1, 0) — the store and
+ * the meta block end identical; out agrees up to rounding, since the new token's score
+ * and weight are taken in fp32 instead of through the 16-bit P of a tile — for the
+ * fish-speech decode step of [PFX "Change"] (step i appends its token and attends the
+ * prefix up to it).  Every block of the launch reads its row's length before the last
+ * one to finish reading advances all rows (a counter in the meta block).  A row that
+ * would pass its capacity sets KVC_DEV_OVERFLOW and is neither written nor attended.
+ * Errors: KVC_ERR_UNSUPPORTED unless the store is LINEAR, 16-bit, served by the decode
+ * kernel (head_dim 64 or 128, heads / kv_heads in {1, 2, 4, 8}) and reads its lengths
+ * from its own meta block (no kvc_use_lengths layout); KVC_ERR_ARG; KVC_ERR_CUDA. */
+int kvc_append_attend_decode(kvc_cache* c, const void* k_new, const void* v_new, const void* q, void* out,
+                             void* stream);
+
 /* kvc_write with RoPE fused into the K half: each K row is rotated at its absolute
  * position before it is stored; V rows are copied unchanged.  Keys stored in a circular
  * cache must carry their absolute-position rotation, applied before the write [RING

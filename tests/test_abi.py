@@ -11,7 +11,7 @@ from diffusion_serving_gb300 import kvc
 
 def test_library_exports_every_declared_function():
     names = kvc.header_functions()
-    assert len(names) == 24
+    assert len(names) == 25
     for n in names:
         assert hasattr(kvc._lib, n), n
     out = subprocess.run(["nm", "-D", "--defined-only", kvc.LIB_PATH], capture_output=True, text=True).stdout
@@ -80,6 +80,7 @@ def test_null_handle_calls_fail_cleanly():
     assert kvc._lib.kvc_attend(None, None, None, 1, 0, None) == kvc.ERR_ARG
     assert kvc._lib.kvc_reset(None, -1, None) == kvc.ERR_ARG
     assert kvc._lib.kvc_get_error(None, None, None) == kvc.ERR_ARG
+    assert kvc._lib.kvc_append_attend_decode(None, None, None, None, None, None) == kvc.ERR_ARG
     assert kvc.kvc_strerror(kvc.ERR_RANGE) == "length out of range"
 
 

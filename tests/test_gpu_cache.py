@@ -324,3 +324,109 @@ def test_captured_append_attend_decode_steps_match_the_oracle():
         assert_close(o1[0], orc.attend(to64(q1[0]), kk, vv), f"step {i}")
     assert c.row_state()[0][3] == T + 20
     assert c.get_error() == 0
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("prefix", [0, 5, 490, 2500])
+def test_fused_append_attend_equals_append_then_attend(dtype, prefix):
+    """kvc_append_attend_decode leaves the same store bytes and row state as kvc_append
+    followed by kvc_attend, and its output, like theirs, matches the oracle over the prefix
+    plus the new token, for prefixes streamed by one block (0, 5, 490 slots) or split (2500), over
+    three consecutive steps with rows of different lengths."""
+    B, H, Hkv, D, cap = 2, 32, 8, 128, 4096
+    fused = kvc.KVCache(B, H, Hkv, D, dtype, "linear", capacity=cap)
+    ref = kvc.KVCache(B, H, Hkv, D, dtype, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(prefix + 3)
+    for c in (fused, ref):
+        c.k_store.zero_()
+        c.v_store.zero_()
+    lens = [prefix, max(prefix - 3, 0) + (7 if prefix else 0)]
+    hist_k, hist_v = [], []
+    for b in range(B):
+        kp = torch.randn(1, lens[b], Hkv, D, device="cuda", generator=g).to(dtype)
+        vp = torch.randn(1, lens[b], Hkv, D, device="cuda", generator=g).to(dtype)
+        hist_k.append(kp[0])
+        hist_v.append(vp[0])
+        for c in (fused, ref):
+            c.k_store[b, :lens[b]] = kp[0]
+            c.v_store[b, :lens[b]] = vp[0]
+            meta = c.meta.view(torch.int32)
+            row = 4 + 4 * b
+            meta[row:row + 4] = torch.tensor([1 if lens[b] else 0, 0, lens[b], lens[b]], dtype=torch.int32)
+    for step in range(3):
+        k = torch.randn(B, 1, Hkv, D, device="cuda", generator=g).to(dtype)
+        v = torch.randn(B, 1, Hkv, D, device="cuda", generator=g).to(dtype)
+        q = torch.randn(B, 1, H, D, device="cuda", generator=g).to(dtype)
+        out = torch.full_like(q, float("nan"))
+        fused.append_attend(k, v, q, out)
+        ref.append(k, v)
+        want = ref.attend(q)
+        torch.cuda.synchronize()
+        assert fused.row_state() == ref.row_state(), f"step {step}"
+        for b in range(B):
+            hist_k[b] = torch.cat([hist_k[b], k[b]])
+            hist_v[b] = torch.cat([hist_v[b], v[b]])
+            o = orc.attend(to64(q[b]), to64(hist_k[b]), to64(hist_v[b]))
+            assert_close(out[b], o, f"step {step} row {b} vs oracle")
+            # the two-launch step's output is checked against the same oracle: both are
+            # within the tolerance of it, the fused one without the 16-bit P of the new key
+            assert_close(want[b], o, f"step {step} row {b}, append + attend vs oracle")
+    assert torch.equal(bits(fused.k_store), bits(ref.k_store)) and torch.equal(bits(fused.v_store), bits(ref.v_store))
+    assert fused.get_error() == 0 and ref.get_error() == 0
+
+
+def test_fused_append_attend_past_capacity_and_unsupported():
+    B, H, Hkv, D, cap = 1, 8, 2, 64, 4
+    c = kvc.KVCache(B, H, Hkv, D, torch.float16, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    for _ in range(cap):
+        k = torch.randn(B, 1, Hkv, D, device="cuda", generator=g).half()
+        q = torch.randn(B, 1, H, D, device="cuda", generator=g).half()
+        c.append_attend(k, k, q)
+    assert c.get_error() == 0
+    before = c.row_state()
+    c.append_attend(k, k, q)                             # slot cap is past the store
+    assert c.get_error() == kvc.DEV_OVERFLOW
+    assert c.row_state() == before
+    ring = kvc.KVCache(1, 8, 2, 64, torch.float16, "circular", sink=4, window=16, chunk=4)
+    with pytest.raises(kvc.KvcError) as e:
+        ring.append_attend(k, k, q)
+    assert e.value.code == kvc.ERR_UNSUPPORTED
+
+
+def test_captured_fused_decode_steps_match_the_oracle():
+    """The fused step captured once and replayed: each replay appends at the next slot
+    and attends the prefix up to it, as the two-launch step does."""
+    B, H, Hkv, D, cap, T = 1, 32, 8, 128, 4096, 234
+    c = kvc.KVCache(B, H, Hkv, D, torch.float16, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(78)
+    kp = torch.randn(B, T, Hkv, D, device="cuda", generator=g).half()
+    vp = torch.randn(B, T, Hkv, D, device="cuda", generator=g).half()
+    c.append(kp, vp)
+    hk, hv = kp[0], vp[0]
+    k1 = torch.zeros(B, 1, Hkv, D, device="cuda").half()
+    v1 = torch.zeros_like(k1)
+    q1 = torch.zeros(B, 1, H, D, device="cuda").half()
+    o1 = torch.empty_like(q1)
+    warm = kvc.KVCache(B, H, Hkv, D, torch.float16, "linear", capacity=cap)
+    warm.append_attend(k1, v1, q1)                   # the kernel's first launch, outside capture
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        c.append_attend(k1, v1, q1, o1, stream=side)
+    torch.cuda.synchronize()
+    assert c.row_state()[0][2] == T                  # capture ran nothing
+    for step in range(4):
+        k1.copy_(torch.randn(B, 1, Hkv, D, device="cuda", generator=g).half())
+        v1.copy_(torch.randn(B, 1, Hkv, D, device="cuda", generator=g).half())
+        q1.copy_(torch.randn(B, 1, H, D, device="cuda", generator=g).half())
+        graph.replay()
+        torch.cuda.synchronize()
+        hk = torch.cat([hk, k1[0]])
+        hv = torch.cat([hv, v1[0]])
+        assert_close(o1[0], orc.attend(to64(q1[0]), to64(hk), to64(hv)), f"replay {step}")
+    assert c.row_state()[0][2] == T + 4
+    assert torch.equal(bits(c.k_store[0, :T + 4]), bits(hk)) and torch.equal(bits(c.v_store[0, :T + 4]), bits(hv))
+    assert c.get_error() == 0
