@@ -230,6 +230,26 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
 
   kvc_pdl_wait();
   kvc_pdl_release();
+  // This block's first tile is the same whatever the row's length turns out to be (tile
+  // `split`: block 0 of a short row streams tiles 0, 1, ... alone, block s of a split row
+  // starts at tile s), and in a LINEAR store its rows do not depend on the meta block:
+  // its load is issued before the length is read, so that the two latencies overlap.  A
+  // tile past the row's end (or past the store, zero-filled) is loaded and skipped.
+  // (Not in the append instantiation, where it measured slower: 6.59 vs 6.42 us a step.)
+  const bool spec = !kApp && g.layout == KVC_LINEAR;
+  if (spec && warp == kWarps && lane == 0) {
+    s_tile[0] = split;                               // published by the arrive below
+    mbar_expect_tx(&full[0], SB);
+#pragma unroll
+    for (int h = 0; h < HB; ++h) {
+      tma_load_4d(&tm_k, &full[0], dsm + h * kHalfBytes, 64 * h, kvh, split * kTile, b);
+      tma_load_4d(&tm_v, &full[0], dsm + (HB + h) * kHalfBytes, 64 * h, kvh, split * kTile, b);
+    }
+  }
+  // a block that leaves before streaming lets that load land first
+  auto leave = [&]() {
+    if (spec && warp == kWarps && lane == 0) mbar_wait(&full[0], 0, &s_wc, false);
+  };
   // Append-then-attend (k_new set, LINEAR): the row's keys are its `filled` stored slots
   // plus the new token, which this launch also writes to slot `filled`; every block reads
   // its row's length, then the last block to arrive advances every row's meta (reserved
@@ -296,7 +316,10 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   } else {
     row_ok = kvc_row_range(g, b, &row0, &len, meta + KVC_META_ERR);
   }
-  if (!row_ok) return;
+  if (!row_ok) {
+    leave();
+    return;
+  }
 
   // Tiles of kTile slots of this row: block `split` takes tiles split, split + nsplit, ...
   // for its first kStages tiles, then claims tiles kStages * nsplit, ... one at a time
@@ -306,7 +329,10 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   // output directly: for a few tiles the split merge (partials, ticket, last-block
   // merge) costs more than one block streaming them.  Uniform per block.
   const bool solo = n_row_tiles <= kSoloTiles;
-  if (solo && split != 0) return;
+  if (solo && split != 0) {
+    leave();
+    return;
+  }
   const int pairs = g.B * g.Hkv;
   const int pair = b * g.Hkv + kvh;
   float* ws_o = ws;                                              // [pairs][nsplit][G][D]
@@ -320,7 +346,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     // ---------------- producer: TMA tiles of K and V into the stage ring ----------------
     if (lane == 0) {
       const int kv_batch = g.layout == KVC_PACKED ? 0 : b;
-      int issued = 0;
+      int issued = spec ? 1 : 0;
       // tile t of this block: static for t < kStages, else claimed.  Claims are issued two
       // tiles ahead, so that their round trips overlap the streaming of two tiles.
       auto claim_for = [&](int t) {   // fixed_tiles: tile t is split + t * nsplit throughout
@@ -329,6 +355,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
       };
       auto step = [&](int t, int tile) {
         const int st = t % kStages;
+        if (t == 0 && spec) return true;                 // issued before the length was read
         if (t >= kStages && !mbar_wait(&empty[st], ((t / kStages) - 1) & 1, abort)) return false;
         if (tile >= n_row_tiles) {                       // no more tiles: tell the consumers
           s_tile[st] = -1;
