@@ -840,13 +840,12 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
 // three S buffers and O (4 x 128 columns), and the QK and PV MMAs come from two warps on
 // different sub-partitions.  S(j + 3) reuses S(j)'s columns once PV(j) has read P(j)
 // from them (s_free), so the loop softmax(j) -> PV(j) -> QK(j + 3) -> softmax(j + 3)
-// spans three tiles and the softmax warps, not the MMA issue, set the pace.  O is read
-// by the epilogue before the next item's first PV (o_free): one bubble per item, which
-// is small on the long rows this kernel is for.
+// spans three tiles.  O is read by the epilogue before the next item's first PV
+// (o_free): one bubble per item, which is small on the long rows this kernel is for.
 // Warps (256 threads): 0 TMA producer of Q (one buffer, reloaded once the item's last
-// QK is done) and K (three-stage ring), 3 TMA producer of V (two-stage ring), 1 QK issuer and TMEM owner, 2 PV issuer (and
-// V-tail zeroing), 4-7 softmax and epilogue of the tile's 128 rows (warp & 3 = TMEM lane
-// quadrant).
+// QK is done) and K (three-stage ring), 3 TMA producer of V (two-stage ring), 1 QK
+// issuer and TMEM owner, 2 PV issuer (and V-tail zeroing), 4-7 softmax and epilogue of
+// the tile's 128 rows (warp & 3 = TMEM lane quadrant).
 constexpr int kSBufs = 3;
 constexpr int kKStages1 = 3, kVStages1 = 2;   // K and V ring depths
 constexpr int kThreads1 = 256;

@@ -273,7 +273,10 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
       int upd = 0;
       if (lane == 0) {
         int prev;
-        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(prev) : "l"(meta + KVC_META_ARRIVE) : "memory");
+        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(meta + KVC_META_ARRIVE)
+                     : "memory");
         upd = prev == (int)(gridDim.x * gridDim.y * gridDim.z) - 1;
       }
       upd = __shfl_sync(kAll, upd, 0);
