@@ -430,3 +430,39 @@ def test_captured_fused_decode_steps_match_the_oracle():
     assert c.row_state()[0][2] == T + 4
     assert torch.equal(bits(c.k_store[0, :T + 4]), bits(hk)) and torch.equal(bits(c.v_store[0, :T + 4]), bits(hv))
     assert c.get_error() == 0
+
+
+@pytest.mark.parametrize("heads,kv_heads,head_dim", [(8, 8, 64), (64, 8, 128), (16, 8, 64)])
+def test_fused_append_attend_other_head_shapes(heads, kv_heads, head_dim):
+    """The append instantiation for one q head per kv head, eight per kv head and
+    head_dim 64: the same store and row state as append + attend, output against the
+    oracle, with one row on one block and one split over several."""
+    B, cap = 2, 2048
+    dtype = torch.bfloat16
+    fused = kvc.KVCache(B, heads, kv_heads, head_dim, dtype, "linear", capacity=cap)
+    ref = kvc.KVCache(B, heads, kv_heads, head_dim, dtype, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(heads + head_dim)
+    for c in (fused, ref):               # past the prefixes both stores hold the same bytes
+        c.k_store.zero_()
+        c.v_store.zero_()
+    lens = (300, 1500)
+    for b, n in enumerate(lens):
+        kp = torch.randn(n, kv_heads, head_dim, device="cuda", generator=g).to(dtype)
+        vp = torch.randn(n, kv_heads, head_dim, device="cuda", generator=g).to(dtype)
+        for c in (fused, ref):
+            c.k_store[b, :n] = kp
+            c.v_store[b, :n] = vp
+            row = 4 + 4 * b
+            c.meta[row:row + 4] = torch.tensor([1, 0, n, n], dtype=torch.int32)
+    k = torch.randn(B, 1, kv_heads, head_dim, device="cuda", generator=g).to(dtype)
+    v = torch.randn(B, 1, kv_heads, head_dim, device="cuda", generator=g).to(dtype)
+    q = torch.randn(B, 1, heads, head_dim, device="cuda", generator=g).to(dtype)
+    out = fused.append_attend(k, v, q)
+    ref.append(k, v)
+    torch.cuda.synchronize()
+    assert fused.row_state() == ref.row_state()
+    assert torch.equal(bits(fused.k_store), bits(ref.k_store)) and torch.equal(bits(fused.v_store), bits(ref.v_store))
+    for b, n in enumerate(lens):
+        o = orc.attend(to64(q[b]), to64(fused.k_store[b, :n + 1]), to64(fused.v_store[b, :n + 1]))
+        assert_close(out[b], o, f"row {b}")
+    assert fused.get_error() == 0
