@@ -13,7 +13,8 @@
 // "pass only active KV cache prefix to SDPA", "Change"); with KVC_CAUSAL the query
 // at absolute position kv_len - n_q + i sees slots <= that position (same section).
 //
-// Work item = two 128-row query tiles (A and B) of one (batch row, q head), sharing
+// The pair kernel, k_attn_tc (the one-tile kernel is described above its definition):
+// work item = two 128-row query tiles (A and B) of one (batch row, q head), sharing
 // every K/V tile it loads.  The kernel is persistent: one CTA per SM walks the items.
 // Warp roles (384 threads):
 //   warps 0, 3  TMA producers (warp 0 the item's Q tiles and K, warp 3 V): tiles of 128
