@@ -203,8 +203,14 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   __shared__ WaitCtl s_wc;
   __shared__ int s_tile[kStages];    // tile index held by each stage, -1: no more tiles
 
-  const int split = blockIdx.x, nsplit = gridDim.x;
-  const int kvh = blockIdx.y, b = blockIdx.z;
+  // Blocks launch in linear order onto the SMs; consecutive blocks take different
+  // (row, kv head) pairs, so that each pair's splits spread over the whole GPU rather
+  // than one region's share of the memory bandwidth.
+  const int nsplit = gridDim.x;
+  const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int n_pairs = gridDim.y * gridDim.z;
+  const int split = lin / n_pairs;
+  const int kvh = (lin % n_pairs) % gridDim.y, b = (lin % n_pairs) / gridDim.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int hq = lane >> 2;          // head row of this lane in the MMA fragments (real if < G)
   const int quad = lane & 3;         // column pair within the fragments
