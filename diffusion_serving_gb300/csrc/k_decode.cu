@@ -241,7 +241,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   // starts at tile s), and in a LINEAR store its rows do not depend on the meta block:
   // its load is issued before the length is read, so that the two latencies overlap.  A
   // tile past the row's end (or past the store, zero-filled) is loaded and skipped.
-  // (Not in the append instantiation, where it measured slower: 6.59 vs 6.42 us a step.)
+  // (Not in the append instantiation, where it measured slower: 5.92 vs 5.68 us a step.)
   const bool spec = !kApp && g.layout == KVC_LINEAR;
   if (spec && warp == kWarps && lane == 0) {
     s_tile[0] = split;                               // published by the arrive below
