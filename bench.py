@@ -899,7 +899,9 @@ def next_rows_bench(kvc, peaks, reps):
     (HBM: K and V read and written once, plus the (cos, sin) rows of the chunk's
     positions), the two-way LSE merge of one chunk's attention outputs (HBM: two partial
     outputs and LSEs read, one written), and attention with LSE output against plain
-    attention over an 8192-slot store."""
+    attention over an 8192-slot store.  The write and the merge rotate over three input
+    sets (each set 87-115 MB, so a set comes back only after more than L2's worth of other
+    traffic)."""
     w = wl.DIT_STREAM
     B, H, Hkv, D, C = w.batch, w.heads, w.kv_heads, w.head_dim, w.chunk
     g = torch.Generator(device="cuda").manual_seed(w.seed)
@@ -918,12 +920,21 @@ def next_rows_bench(kvc, peaks, reps):
     res = {}
     cache = kvc.KVCache(B, H, Hkv, D, torch.bfloat16, "circular", sink=w.sink, window=w.window, chunk=C)
     cache.advance()
-    k = torch.randn(B, C, Hkv, D, device="cuda", generator=g).bfloat16()
-    v = torch.randn(B, C, Hkv, D, device="cuda", generator=g).bfloat16()
+    kv_sets = [(torch.randn(B, C, Hkv, D, device="cuda", generator=g).bfloat16(),
+                torch.randn(B, C, Hkv, D, device="cuda", generator=g).bfloat16()) for _ in range(3)]
     table = wl.rope_table(w.window, D).cuda()
-    t_plain = time_it(lambda: cache.write(k, v))
-    t_rope = time_it(lambda: cache.write_rope(k, v, table))
+    turn = [0]
+
+    def rotating(fn, sets):
+        def call():
+            fn(*sets[turn[0] % len(sets)])
+            turn[0] += 1
+        return call
+
+    t_plain = time_it(rotating(lambda k, v: cache.write(k, v), kv_sets))
+    t_rope = time_it(rotating(lambda k, v: cache.write_rope(k, v, table), kv_sets))
     assert cache.get_error() == 0
+    k = kv_sets[0][0]
     nbytes = 2 * 2 * k.numel() * k.element_size() + C * (D // 2) * 2 * 4
     res["write_rope"] = {"us": round(t_rope * 1e6, 2), "GB/s": round(nbytes / t_rope / 1e9, 1),
                          "frac": round(nbytes / t_rope / 1e9 / peaks["hbm"], 4), "bytes": nbytes,
@@ -931,13 +942,14 @@ def next_rows_bench(kvc, peaks, reps):
     cache.close()
 
     rows = B * C * H
-    oa = torch.randn(rows, D, device="cuda", generator=g).bfloat16()
-    ob = torch.randn(rows, D, device="cuda", generator=g).bfloat16()
-    la = torch.randn(rows, device="cuda", generator=g)
-    lb = torch.randn(rows, device="cuda", generator=g)
-    out = torch.empty_like(oa)
-    lo = torch.empty_like(la)
-    t_merge = time_it(lambda: kvc.kvc_merge(torch.bfloat16, rows, D, oa, la, ob, lb, out, lo))
+    merge_sets = [(torch.randn(rows, D, device="cuda", generator=g).bfloat16(),
+                   torch.randn(rows, device="cuda", generator=g),
+                   torch.randn(rows, D, device="cuda", generator=g).bfloat16(),
+                   torch.randn(rows, device="cuda", generator=g),
+                   torch.empty(rows, D, device="cuda", dtype=torch.bfloat16),
+                   torch.empty(rows, device="cuda")) for _ in range(3)]
+    t_merge = time_it(rotating(lambda oa, la, ob, lb, out, lo:
+                               kvc.kvc_merge(torch.bfloat16, rows, D, oa, la, ob, lb, out, lo), merge_sets))
     nbytes = rows * (3 * D * 2 + 3 * 4)
     res["merge"] = {"rows": rows, "us": round(t_merge * 1e6, 2), "GB/s": round(nbytes / t_merge / 1e9, 1),
                     "frac": round(nbytes / t_merge / 1e9 / peaks["hbm"], 4), "bytes": nbytes}

@@ -262,6 +262,40 @@ def test_cross_attention_small(lens):
         assert_close(o_unmasked[b], ref_u, f"unmasked b{b}")
 
 
+def test_cross_attention_many_items():
+    """Ragged cross-attention with 1280 tile pairs (over 8 per SM, so every persistent CTA
+    walks many items of both lengths): every row against the oracle."""
+    Lq, H, lens = 2 * 128 * 80, 8, (200, 60)
+    q, k, v, o_packed, o_kvlen, o_unmasked = cross_arms(Lq, H, lens)
+    assert torch.equal(bits(o_packed), bits(o_kvlen))
+    for b in range(2):
+        ref = orc.attend(to64(q[b]), to64(k[b, :lens[b]]), to64(v[b, :lens[b]]))
+        assert_close(o_packed[b], ref, f"packed b{b}")
+        ref_u = orc.attend(to64(q[b]), to64(k[b]), to64(v[b]))
+        assert_close(o_unmasked[b], ref_u, f"unmasked b{b}")
+
+
+def test_causal_short_store_many_items():
+    """Causal rows of different lengths in a short store (the pair kernel) with 1280 items
+    and grouped query heads: the diagonal falls on a different tile and column in each
+    row, and the V tail rows zeroed for one item's partial tile are reloaded or re-zeroed
+    for the next item that reads that tile."""
+    lens = (384, 400, 450, 512, 385, 500, 511, 449)
+    B, H, Hkv, D, n_q, cap = len(lens), 80, 8, 128, 384, 512
+    cache = kvc.KVCache(B, H, Hkv, D, torch.bfloat16, "linear", capacity=cap)
+    g = torch.Generator(device="cuda").manual_seed(1280)
+    cache.k_store.normal_(generator=g)
+    cache.v_store.normal_(generator=g)
+    cache.set_lengths(kv_len=torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    q = torch.randn(B, n_q, H, D, device="cuda", generator=g).bfloat16()
+    out = cache.attend(q, flags=kvc.CAUSAL)
+    for b, n in enumerate(lens):
+        ref = orc.attend(to64(q[b]), to64(cache.k_store[b, :n]), to64(cache.v_store[b, :n]), causal=True,
+                         q_pos0=n - n_q)
+        assert_close(out[b], ref, f"causal row {b} kv_len {n}")
+    assert cache.get_error() == 0
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("skew", list(wl.CROSS_SKEWS))
 def test_cross_attention_full_size(skew):
