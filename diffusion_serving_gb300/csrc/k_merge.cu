@@ -28,18 +28,21 @@ __device__ __forceinline__ void st(float* p, float x) { *p = x; }
 __device__ __forceinline__ void st(__half* p, float x) { *p = __float2half_rn(x); }
 __device__ __forceinline__ void st(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-// weights of the two halves and the merged LSE of one row
+// weights of the two halves and the merged LSE of one row: with mx the larger input,
+// e^(La - mx) and e^(Lb - mx) are 1 and e = e^(-|La - Lb|), so one exponential, one
+// logarithm and one reciprocal serve the row
 __device__ __forceinline__ void merge_weights(float a, float b, float& wa, float& wb, float& L) {
   const float mx = fmaxf(a, b);
   wa = 0.f;
   wb = 0.f;
   L = -INFINITY;
   if (mx != -INFINITY) {
-    const float ea = expf(a - mx), eb = expf(b - mx);   // one of them is 1
-    const float tot = ea + eb;
+    const float e = expf(fminf(a, b) - mx);
+    const float tot = 1.f + e;
+    const float inv = 1.f / tot;
     L = mx + logf(tot);
-    wa = ea / tot;
-    wb = eb / tot;
+    wa = a >= b ? inv : e * inv;
+    wb = a >= b ? e * inv : inv;
   }
 }
 
@@ -117,7 +120,7 @@ struct Chunk<__nv_bfloat16> : Chunk16<__nv_bfloat162, b2_to_f2, f2_to_b2> {};
 // chunks per row).  Grid-stride over groups of kMergeUnroll chunks spaced one grid apart,
 // so each of a group's loads is coalesced across the warp.
 template <typename T>
-__global__ void __launch_bounds__(kMergeThreads, 3)
+__global__ void __launch_bounds__(kMergeThreads, 4)
 k_merge_vec(int64_t chunks, int row_shift, const uint4* oa, const float* __restrict__ la, const uint4* ob,
             const float* __restrict__ lb, uint4* out, float* __restrict__ lse) {
   kvc_pdl_wait();
