@@ -807,13 +807,18 @@ def ours(args):
         for e in used + fetched:
             e.record(comp)
 
+        turn = [0]   # device slots in use order, counted across steps: a step's first chunks
+                     # take the slots its predecessor freed first, not the ones its last
+                     # (longest) attends still read
+
         def e2e_step():
             cache.reset(stream=comp)
             i = 0
             for c in range(w.n_chunks):
                 cache.advance(stream=comp)
                 for r in range(w.rewrites):
-                    slot = i % nslot
+                    slot = turn[0] % nslot
+                    turn[0] += 1
                     q, k, v = dev[slot]
                     hq, hk, hv = host[i % len(host)]
                     with torch.cuda.stream(s_in):
