@@ -155,3 +155,47 @@ def test_merge_paths_match_oracle(case):
     assert torch.all(out[7] == 0) and torch.isneginf(lo[7])
     fin = np.isfinite(ref_l)
     assert np.allclose(lo.double().cpu().numpy()[fin], ref_l[fin], rtol=1e-6, atol=1e-5)
+
+
+UNIT_ROUNDOFF = {torch.float32: 2.0 ** -24, torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+# half the spacing of the type's subnormals: the absolute rounding error below its normal range
+SUBNORMAL_HALF_STEP = {torch.float32: 2.0 ** -150, torch.float16: 2.0 ** -25, torch.bfloat16: 2.0 ** -134}
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [128, 72])                 # 16-byte chunk path, scalar path
+@pytest.mark.parametrize("alias", ["none", "a", "b"])   # out written over o_a or o_b
+def test_merge_dtypes_and_in_place(dtype, D, alias):
+    """The merge in every store type, on both kernel paths, into a separate buffer and in
+    place over either input: the oracle's merge within one rounding to the type plus the
+    fp32 weights' error (or half a subnormal step, for results below the type's normal
+    range), rows without keys 0 and -inf."""
+    rows = 777
+    g = torch.Generator(device="cuda").manual_seed(D + len(alias))
+    oa = torch.randn(rows, D, device="cuda", generator=g).to(dtype)
+    ob = torch.randn(rows, D, device="cuda", generator=g).to(dtype)
+    la = torch.randn(rows, device="cuda", generator=g) * 4
+    lb = torch.randn(rows, device="cuda", generator=g) * 4
+    la[3] = float("-inf")
+    la[9] = lb[9] = float("-inf")
+    oa64, ob64 = to64(oa), to64(ob)
+    la64, lb64 = la.double().cpu().numpy(), lb.double().cpu().numpy()
+    out = {"none": torch.empty_like(oa), "a": oa, "b": ob}[alias]
+    lo = torch.empty_like(la)
+    kvc.kvc_merge(dtype, rows, D, oa, la, ob, lb, out, lo)
+    torch.cuda.synchronize()
+    ref_o, ref_l = orc.merge_lse(oa64, la64, ob64, lb64)
+    safe = np.where(np.isfinite(ref_l), ref_l, 0.0)
+    wa = np.where(np.isfinite(la64), np.exp(la64 - safe), 0.0)[:, None]
+    wb = np.where(np.isfinite(lb64), np.exp(lb64 - safe), 0.0)[:, None]
+    mag = np.abs(wa * oa64) + np.abs(wb * ob64)
+    got = to64(out)
+    bound_o = UNIT_ROUNDOFF[dtype] * np.abs(ref_o) + 2.0 ** -19 * mag + SUBNORMAL_HALF_STEP[dtype]
+    err = np.abs(got - ref_o)
+    assert np.all(err <= bound_o), f"worst {np.unravel_index(np.argmax(err - bound_o), err.shape)}"
+    assert torch.all(out[9] == 0) and torch.isneginf(lo[9])
+    fin = np.isfinite(ref_l)
+    with np.errstate(invalid="ignore"):
+        bound = merge_lse_error_bound(la64, lb64, np.zeros(rows), np.zeros(rows))
+    bound = np.where(np.isfinite(la64) & np.isfinite(lb64), bound, 2.0 ** -20 + 2.0 ** -23 * np.abs(ref_l))
+    assert np.all(np.abs(lo.double().cpu().numpy()[fin] - ref_l[fin]) <= bound[fin])
