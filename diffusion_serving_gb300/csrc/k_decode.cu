@@ -7,7 +7,8 @@
 // materialised).  The query is the newest token, so no mask applies.
 //
 // Grid (splits, Hkv, B); the grid depends only on the shape, so a captured graph
-// replays at any length.  A row's kv_len slots form tiles of kTile slots.  A row of at
+// replays at any length.  A block takes its (row, kv head) pair and its split from its
+// linear launch index, pairs interleaved.  A row's kv_len slots form tiles of kTile slots.  A row of at
 // most kSoloTiles tiles is streamed by one block, which writes the output directly.
 // Otherwise each block streams some of its (row, kv head)'s tiles: kStages fixed ones
 // first, then tiles claimed one at a time from a counter, so faster blocks take more.  A producer warp
@@ -20,6 +21,12 @@
 // workspace; the last block of each (row, kv head) to finish (a ticket counter, left
 // at zero for the next call with the claim counter) merges the partials:
 // O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
+//
+// The append instantiation is a whole decode step in one launch: each row's prefix is
+// its filled count, the new token's key and value come from the caller's buffers and
+// join the final merge in fp32 (score and weight), block 0 of each (row, kv head)
+// stores them at the row's next slot, and the last block to arrive on a counter in the
+// meta block advances every row's counters.
 #include "kvc_internal.h"
 
 #include <cuda_bf16.h>
