@@ -39,7 +39,7 @@ namespace {
 constexpr int kWarps = 7;                   // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
 constexpr int kTile = kWarps * 16;          // 112 slots per stage, 16 per consumer warp
-constexpr int kSoloTiles = 6;               // rows of at most this many tiles: one block, no split merge
+constexpr int kSoloTiles = 5;               // rows of at most this many tiles: one block, no split merge
 constexpr int kStages = 4;                  // 4 x 56 KB in flight per SM (bandwidth x loaded latency)
 constexpr uint64_t kTimeoutNs = 500000000ull;
 
@@ -170,6 +170,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, const __nv_bfloat1
 }
 __device__ __forceinline__ void store_out(__half* p, float x) { *p = __float2half_rn(x); }
 __device__ __forceinline__ void store_out(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+// a += w * x, element by element; and four outputs x * inv stored from p on
+__device__ __forceinline__ void acc4(float4& a, float w, const float4& x) {
+  a.x = fmaf(w, x.x, a.x);
+  a.y = fmaf(w, x.y, a.y);
+  a.z = fmaf(w, x.z, a.z);
+  a.w = fmaf(w, x.w, a.w);
+}
+template <typename T>
+__device__ __forceinline__ void store_out4(T* p, const float4& x, float inv) {
+  store_out(p, x.x * inv);
+  store_out(p + 1, x.y * inv);
+  store_out(p + 2, x.z * inv);
+  store_out(p + 3, x.w * inv);
+}
 __device__ __forceinline__ float load_f(const __half* p) { return __half2float(*p); }
 __device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
 
@@ -556,32 +570,32 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
       if (lse != nullptr) lse[(int64_t)b * g.H + kvh * G + gg] = (M + log2f(L)) * 0.6931471805599453f;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-      const int gg = e / D, d = e - gg * D;
+    for (int v = threadIdx.x; v < G * D / 4; v += blockDim.x) {   // 4 outputs of one head each
+      const int gg = (4 * v) / D, d = 4 * v - gg * D;
       const float M = s_max[gg];
-      float a = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
         const float mw = s_ml[w][gg][0];
-        if (mw != -INFINITY) a = fmaf(ex2(mw - M), s_acc[w][gg][d], a);
+        if (mw != -INFINITY) acc4(a, ex2(mw - M), *reinterpret_cast<const float4*>(&s_acc[w][gg][d]));
       }
-      if (app) a = fmaf(s_pnew[gg], s_vnew[d], a);
-      store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, a * s_inv[gg]);
+      if (app) acc4(a, s_pnew[gg], make_float4(s_vnew[d], s_vnew[d + 1], s_vnew[d + 2], s_vnew[d + 3]));
+      store_out4(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, a, s_inv[gg]);
     }
     return;
   }
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
-    const int gg = e / D, d = e - gg * D;
+  for (int v = threadIdx.x; v < G * D / 4; v += blockDim.x) {     // 4 outputs of one head each
+    const int gg = (4 * v) / D, d = 4 * v - gg * D;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[w][gg][0]);
-    float a = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       const float mw = s_ml[w][gg][0];
-      if (mw != -INFINITY) a = fmaf(ex2(mw - M), s_acc[w][gg][d], a);
+      if (mw != -INFINITY) acc4(a, ex2(mw - M), *reinterpret_cast<const float4*>(&s_acc[w][gg][d]));
     }
-    ws_o[((int64_t)pair * nsplit + split) * G * D + e] = a;
+    reinterpret_cast<float4*>(ws_o + ((int64_t)pair * nsplit + split) * G * D)[v] = a;
   }
   if (threadIdx.x < G) {
     const int gg = threadIdx.x;
@@ -606,21 +620,23 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   if (!s_last) return;
 
   // ---- merge the splits (last block of this (b, kv head)) -------------------
-  // This thread's outputs e = threadIdx.x + i * blockDim.x load their first kPre split
-  // partials at once (one L2 round trip, in flight while the weights are formed); the
-  // (m_s, l_s) of every used split and head go to shared memory (the stage ring is free
-  // now), weights 2^(m_s - M) per head, then O = sum_s w_s O_s / sum_s w_s l_s.
-  constexpr int kOut = (G * D + kThreads - 1) / kThreads;         // outputs per thread
-  constexpr int kPre = 48 / kOut;                                  // splits prefetched per output
+  // Thread t owns the 16-byte output groups v = t + i * blockDim.x (outputs 4v .. 4v + 3,
+  // one head) and loads their first kPre split partials at once, 16 bytes a load (one L2
+  // round trip, in flight while the weights are formed); the (m_s, l_s) of every used
+  // split and head go to shared memory (the stage ring is free now), weights 2^(m_s - M)
+  // per head, then O = sum_s w_s O_s / sum_s w_s l_s.
+  constexpr int kVec = G * D / 4;                                  // 16-byte groups of outputs
+  constexpr int kOut4 = (kVec + kThreads - 1) / kThreads;         // groups per thread
+  constexpr int kPre = 24 / kOut4;                                 // splits prefetched per group
   const int used = min(nsplit, n_row_tiles);                     // blocks past the tile count took none
-  const float* ws_pair = ws_o + (int64_t)pair * nsplit * G * D;
-  float pre[kOut][kPre];
+  const float4* ws_pair = reinterpret_cast<const float4*>(ws_o + (int64_t)pair * nsplit * G * D);
+  float4 pre[kOut4][kPre];
 #pragma unroll
-  for (int i = 0; i < kOut; ++i) {
-    const int e = threadIdx.x + i * kThreads;
+  for (int i = 0; i < kOut4; ++i) {
+    const int v = threadIdx.x + i * kThreads;
 #pragma unroll
     for (int k = 0; k < kPre; ++k)
-      pre[i][k] = (e < G * D && k < used) ? __ldcg(ws_pair + (int64_t)k * G * D + e) : 0.f;
+      pre[i][k] = (v < kVec && k < used) ? __ldcg(ws_pair + (int64_t)k * kVec + v) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float* sw = reinterpret_cast<float*>(dsm);                     // [G][used] weights
   float* sl = sw + G * used;                                     // [G][used] sums
@@ -656,18 +672,18 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   }
   __syncthreads();
 #pragma unroll
-  for (int i = 0; i < kOut; ++i) {
-    const int e = threadIdx.x + i * kThreads;
-    if (e >= G * D) break;
-    const int gg = e / D, d = e - gg * D;
+  for (int i = 0; i < kOut4; ++i) {
+    const int v = threadIdx.x + i * kThreads;
+    if (v >= kVec) break;
+    const int gg = (4 * v) / D, d = 4 * v - gg * D;
     const float* wrow = sw + gg * used;
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < kPre; ++k)
-      if (k < used) o[k & 3] = fmaf(wrow[k], pre[i][k], o[k & 3]);
-    for (int k = kPre; k < used; ++k) o[k & 3] = fmaf(wrow[k], __ldcg(ws_pair + (int64_t)k * G * D + e), o[k & 3]);
-    if (app) o[0] = fmaf(s_pnew[gg], s_vnew[d], o[0]);
-    store_out(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, ((o[0] + o[1]) + (o[2] + o[3])) * s_inv[gg]);
+      if (k < used) acc4(o, wrow[k], pre[i][k]);
+    for (int k = kPre; k < used; ++k) acc4(o, wrow[k], __ldcg(ws_pair + (int64_t)k * kVec + v));
+    if (app) acc4(o, s_pnew[gg], make_float4(s_vnew[d], s_vnew[d + 1], s_vnew[d + 2], s_vnew[d + 3]));
+    store_out4(out + ((int64_t)b * g.H + kvh * G + gg) * D + d, o, s_inv[gg]);
   }
   if (threadIdx.x == 0) {           // every block of the pair is past both counters
     tickets[pair] = 0;
