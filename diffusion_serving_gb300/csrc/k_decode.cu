@@ -41,6 +41,7 @@ constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
 constexpr int kTile = kWarps * 16;          // 112 slots per stage, 16 per consumer warp
 constexpr int kSoloTiles = 5;               // rows of at most this many tiles: one block, no split merge
 constexpr int kStages = 4;                  // 4 x 56 KB in flight per SM (bandwidth x loaded latency)
+constexpr int kSplitRegs = 5;               // the split merge holds up to 32 x 5 splits' (m, l) in registers
 constexpr uint64_t kTimeoutNs = 500000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -638,26 +639,38 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     for (int k = 0; k < kPre; ++k)
       pre[i][k] = (v < kVec && k < used) ? __ldcg(ws_pair + (int64_t)k * kVec + v) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  // One warp per head: lane s takes split s's (m_s, l_s) straight into registers (up to
+  // kSplitRegs splits), forms M and the weights, and leaves them in shared memory for
+  // the output groups: one barrier between the loads and the outputs.
   float* sw = reinterpret_cast<float*>(dsm);                     // [G][used] weights
-  float* sl = sw + G * used;                                     // [G][used] sums
-  for (int e = threadIdx.x; e < G * used; e += blockDim.x) {
-    const int gg = e / used, s = e - gg * used;
-    sw[e] = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2);
-    sl[e] = __ldcg(ws_ml + (((int64_t)pair * nsplit + s) * G + gg) * 2 + 1);
-  }
-  __syncthreads();
   for (int gg = warp; gg < G; gg += kWarps + 1) {
+    float mr[kSplitRegs], lr[kSplitRegs];
+#pragma unroll
+    for (int j = 0; j < kSplitRegs; ++j) {
+      const int sp = lane + 32 * j;
+      mr[j] = -INFINITY;
+      lr[j] = 0.f;
+      if (sp < used) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(ws_ml + (((int64_t)pair * nsplit + sp) * G + gg) * 2));
+        mr[j] = ml.x;
+        lr[j] = ml.y;
+      }
+    }
     float M = -INFINITY;
-    for (int s = lane; s < used; s += 32) M = fmaxf(M, sw[gg * used + s]);
+#pragma unroll
+    for (int j = 0; j < kSplitRegs; ++j) M = fmaxf(M, mr[j]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (app) M = fmaxf(M, s_snew[gg]);
     float L = 0.f;
-    for (int s = lane; s < used; s += 32) {
-      const float ms = sw[gg * used + s];
-      const float wgt = ms == -INFINITY ? 0.f : ex2(ms - M);
-      sw[gg * used + s] = wgt;
-      L = fmaf(wgt, sl[gg * used + s], L);
+#pragma unroll
+    for (int j = 0; j < kSplitRegs; ++j) {
+      const int sp = lane + 32 * j;
+      if (sp < used) {
+        const float wgt = mr[j] == -INFINITY ? 0.f : ex2(mr[j] - M);
+        sw[gg * used + sp] = wgt;
+        L = fmaf(wgt, lr[j], L);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
@@ -708,6 +721,7 @@ cudaError_t launch_dg(kvc_cache* c, const void* q, void* out, float* lse, int fi
     return cudaFuncSetAttribute(k_decode<T, D, G, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   }
   const kvc_config& cfg = c->cfg;
+  if (c->dec_splits > 32 * kSplitRegs) return cudaErrorInvalidValue;   // the merge's register budget
   kvc_geom g{cfg.batch, cfg.heads, cfg.kv_heads, cfg.head_dim, c->cap, cfg.layout, c->lens};
   dim3 grid(c->dec_splits, cfg.kv_heads, cfg.batch);
   const float sl2 = c->scale * 1.4426950408889634f;
