@@ -8,8 +8,9 @@
 //
 // Grid (splits, Hkv, B); the grid depends only on the shape, so a captured graph
 // replays at any length.  A block takes its (row, kv head) pair and its split from its
-// linear launch index, pairs interleaved.  A row's kv_len slots form tiles of kTile slots.  A row of at
-// most kSoloTiles tiles is streamed by one block, which writes the output directly.
+// linear launch index, pairs interleaved.  A row's kv_len slots form tiles of kTile
+// slots.  A row of at most kSoloTiles tiles (kSoloTilesAppend in the append
+// instantiation) is streamed by one block, which writes the output directly.
 // Otherwise each block streams some of its (row, kv head)'s tiles: kStages fixed ones
 // first, then tiles claimed one at a time from a counter, so faster blocks take more.  A producer warp
 // moves each tile into a ring of shared-memory stages with TMA (128-byte-swizzled
@@ -39,7 +40,10 @@ namespace {
 constexpr int kWarps = 7;                   // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32; // + one producer warp
 constexpr int kTile = kWarps * 16;          // 112 slots per stage, 16 per consumer warp
-constexpr int kSoloTiles = 5;               // rows of at most this many tiles: one block, no split merge
+// rows of at most this many tiles: one block, no split merge (the append instantiation's
+// split path starts later, without the speculative first tile, so it splits one tile later)
+constexpr int kSoloTiles = 4;
+constexpr int kSoloTilesAppend = 5;
 constexpr int kStages = 4;                  // 4 x 56 KB in flight per SM (bandwidth x loaded latency)
 constexpr int kSplitRegs = 5;               // the split merge holds up to 32 x 5 splits' (m, l) in registers
 constexpr uint64_t kTimeoutNs = 500000000ull;
@@ -359,7 +363,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   // A short row is streamed by block 0 of its (row, kv head) alone, which writes the
   // output directly: for a few tiles the split merge (partials, ticket, last-block
   // merge) costs more than one block streaming them.  Uniform per block.
-  const bool solo = n_row_tiles <= kSoloTiles;
+  const bool solo = n_row_tiles <= (kApp ? kSoloTilesAppend : kSoloTiles);
   if (solo && split != 0) {
     leave();
     return;

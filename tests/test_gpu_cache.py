@@ -327,12 +327,12 @@ def test_captured_append_attend_decode_steps_match_the_oracle():
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("prefix", [0, 5, 111, 112, 490, 559, 560, 561, 672, 673, 2500])
+@pytest.mark.parametrize("prefix", [0, 5, 111, 112, 447, 448, 449, 490, 560, 561, 672, 673, 2500])
 def test_fused_append_attend_equals_append_then_attend(dtype, prefix):
     """kvc_append_attend_decode leaves the same store bytes and row state as kvc_append
     followed by kvc_attend, and its output, like theirs, matches the oracle over the prefix
-    plus the new token, for prefixes streamed by one block (up to 560 slots: 5 tiles of
-    112) or split (561 and longer), on and beside tile edges and the block-count
+    plus the new token, for prefixes streamed by one block (up to 448 slots: 4 tiles of
+    112) or split (449 and longer), on and beside tile edges and the block-count
     threshold, over three consecutive steps with rows of different lengths."""
     B, H, Hkv, D, cap = 2, 32, 8, 128, 4096
     fused = kvc.KVCache(B, H, Hkv, D, dtype, "linear", capacity=cap)
