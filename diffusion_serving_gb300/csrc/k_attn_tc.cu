@@ -187,6 +187,7 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until at most one committed bulk group still reads its shared-memory source
 __device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // wait until every committed bulk group has completed its writes
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -689,10 +690,11 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
     bool pend = false;
     int pend_b = 0, pend_h = 0, pend_grow = 0, pend_row = 0;
     float pend_m = 0.f, pend_l = 0.f;
-    // The pending item's output: once its last PV is done, O / l leaves TMEM 32 columns at
-    // a time through 64-byte-swizzled staging (16-byte chunk c of row r at chunk
-    // c ^ ((r >> 1) & 3), conflict-free) and one TMA store per 32 columns; rows past n_q
-    // are clipped by the map.  Also the LSE of the row.
+    // The pending item's output: once its last PV is done, O / l leaves TMEM 64 columns at
+    // a time through the warp's two 64-byte-swizzled staging buffers (16-byte chunk c of
+    // row r at chunk c ^ ((r >> 1) & 3), conflict-free), one proxy fence and two 32-column
+    // TMA stores per 64 columns; rows past n_q are clipped by the map.  Also the LSE of
+    // the row.
     auto o_flush = [&]() {
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&sm.o_done[t], (n_items_done - 1) & 1, abort));
       if (!ok) return;
@@ -701,29 +703,39 @@ k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
       if (p.lse != nullptr && pend_row < p.n_q)   // m and l are in the exp2 domain of scale * q.k
         p.lse[((int64_t)pend_b * p.n_q + pend_row) * g.H + pend_h] =
             pend_l > 0.f ? (pend_m + log2f(pend_l)) * 0.6931471805599453f : -INFINITY;
+      // two halves of 64 columns: both staging buffers filled, one proxy fence, two stores
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t orow[32], pk[16];
-        tmem_ld32(o_addr + q4 * 32, orow);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t orow[64];
+        tmem_ld32(o_addr + hf * 64, orow);
+        tmem_ld32(o_addr + hf * 64 + 32, orow + 32);
         tmem_ld_wait();
         reg_fence32(orow);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 y = __fmul2_rn(make_float2(__uint_as_float(orow[2 * i]), __uint_as_float(orow[2 * i + 1])),
-                                      make_float2(inv, inv));
-          pk[i] = pack2<kBf16>(y.x, y.y);
-        }
-        uint8_t* buf = stage + (q4 & 1) * kStageBytes;
-        if (lane == 0) bulk_wait_read1();              // the store that last read buf is done with it
+        reg_fence32(orow + 32);
+        if (lane == 0) bulk_wait_read0();              // the stores that last read both buffers are done
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
-              make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 y = __fmul2_rn(
+                make_float2(__uint_as_float(orow[c2 * 32 + 2 * i]), __uint_as_float(orow[c2 * 32 + 2 * i + 1])),
+                make_float2(inv, inv));
+            pk[i] = pack2<kBf16>(y.x, y.y);
+          }
+          uint8_t* buf = stage + c2 * kStageBytes;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
+                make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) {
-          tma_store_4d(&tm_o, buf, q4 * 32, pend_h, pend_grow, pend_b);
+          const int c1 = 2 * hf + 1;                   // the half's second 32-column box
+          tma_store_4d(&tm_o, stage, hf * 64, pend_h, pend_grow, pend_b);
+          tma_store_4d(&tm_o, stage + kStageBytes, c1 * 32, pend_h, pend_grow, pend_b);
           bulk_commit();
         }
       }
