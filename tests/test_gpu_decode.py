@@ -22,8 +22,9 @@ if torch.cuda.is_available():
     from diffusion_serving_gb300 import kvc
 
 # lengths: a single slot, a warp slice, a ragged warp slice, one tile, one past a tile,
-# several tiles with a ragged tail
-LENS = (1, 16, 17, 112, 113, 1000, 2900)
+# the last length one block streams alone and the first one split over blocks (4 tiles
+# and one slot more), one past 5 tiles, several tiles with a ragged tail
+LENS = (1, 16, 17, 112, 113, 448, 449, 561, 1000, 2900)
 
 
 def linear_cache(dtype, H, Hkv, D, lens, cap, seed):
