@@ -627,9 +627,9 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   // ---- merge the splits (last block of this (b, kv head)) -------------------
   // Thread t owns the 16-byte output groups v = t + i * blockDim.x (outputs 4v .. 4v + 3,
   // one head) and loads their first kPre split partials at once, 16 bytes a load (one L2
-  // round trip, in flight while the weights are formed); the (m_s, l_s) of every used
-  // split and head go to shared memory (the stage ring is free now), weights 2^(m_s - M)
-  // per head, then O = sum_s w_s O_s / sum_s w_s l_s.
+  // round trip, in flight while the weights are formed); the weights 2^(m_s - M) of each
+  // head go to shared memory (the stage ring is free now), then
+  // O = sum_s w_s O_s / sum_s w_s l_s.
   constexpr int kVec = G * D / 4;                                  // 16-byte groups of outputs
   constexpr int kOut4 = (kVec + kThreads - 1) / kThreads;         // groups per thread
   constexpr int kPre = 24 / kOut4;                                 // splits prefetched per group
