@@ -47,6 +47,8 @@ k_attn_simt(const T* __restrict__ q, T* __restrict__ out, const T* __restrict__ 
   __shared__ float sV[kTile][D];
   __shared__ float sQ[kRowsPerBlock][D];
 
+  kvc_pdl_wait();      // launched as a programmatic dependent: nothing is read before this
+  kvc_pdl_release();
   const int b = blockIdx.z, h = blockIdx.y;
   const int i0 = blockIdx.x * kRowsPerBlock;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -154,12 +156,10 @@ cudaError_t launch_t(kvc_cache* c, const void* q, void* out, int n_q, bool causa
   dim3 grid((n_q + kRowsPerBlock - 1) / kRowsPerBlock, cfg.heads, cfg.batch);
   const float sl2 = c->scale * 1.4426950408889634f;
   if (cfg.head_dim == 64)
-    k_attn_simt<T, 64><<<grid, kWarps * 32, 0, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta, g,
-                                                    n_q, causal ? 1 : 0, sl2, lse);
-  else
-    k_attn_simt<T, 128><<<grid, kWarps * 32, 0, s>>>((const T*)q, (T*)out, (const T*)c->k, (const T*)c->v, c->meta,
-                                                     g, n_q, causal ? 1 : 0, sl2, lse);
-  return cudaGetLastError();
+    return kvc_launch_pdl(k_attn_simt<T, 64>, grid, dim3(kWarps * 32), 0, s, (const T*)q, (T*)out, (const T*)c->k,
+                          (const T*)c->v, c->meta, g, n_q, causal ? 1 : 0, sl2, lse);
+  return kvc_launch_pdl(k_attn_simt<T, 128>, grid, dim3(kWarps * 32), 0, s, (const T*)q, (T*)out, (const T*)c->k,
+                        (const T*)c->v, c->meta, g, n_q, causal ? 1 : 0, sl2, lse);
 }
 
 }  // namespace
