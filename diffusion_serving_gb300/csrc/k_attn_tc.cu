@@ -185,8 +185,6 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void*
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// wait until at most one committed bulk group still reads its shared-memory source
-__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // wait until every committed bulk group has completed its writes
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -448,6 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_attn_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
           int32_t* __restrict__ meta, TcParams p) {
+  kvc_pdl_wait();   // launched as a programmatic dependent: nothing is read before this
+  kvc_pdl_release();
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -912,6 +912,8 @@ __global__ void __launch_bounds__(kThreads1, 1)
 k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
           int32_t* __restrict__ meta, TcParams p) {
+  kvc_pdl_wait();   // launched as a programmatic dependent: nothing is read before this
+  kvc_pdl_release();
   extern __shared__ uint8_t smem_raw[];
   Smem1& sm = *reinterpret_cast<Smem1*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1225,9 +1227,10 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
         tmem_ld_wait();
         reg_fence32(orow);
         reg_fence32(orow + 32);
+        if (lane == 0) bulk_wait_read0();              // the stores that last read both buffers are done
+        __syncwarp();
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          const int q4 = 2 * q2 + c2;
+        for (int c2 = 0; c2 < 2; ++c2) {               // both staging buffers, then one proxy fence
           const uint32_t* oc = orow + 32 * c2;
           uint32_t pk[16];
 #pragma unroll
@@ -1237,18 +1240,18 @@ k_attn_1q(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUte
             pk[i] = pack2<kBf16>(y.x, y.y);
           }
           uint8_t* buf = stage + c2 * kStageBytes;
-          if (lane == 0) bulk_wait_read1();
-          __syncwarp();
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<uint4*>(buf + lane * 64 + ((i ^ ((lane >> 1) & 3)) * 16)) =
                 make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_4d(&tm_o, buf, q4 * 32, I.h, grow, I.b);
-            bulk_commit();
-          }
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+          const int c1 = 2 * q2 + 1;                   // the half's second 32-column box
+          tma_store_4d(&tm_o, stage, q2 * 64, I.h, grow, I.b);
+          tma_store_4d(&tm_o, stage + kStageBytes, c1 * 32, I.h, grow, I.b);
+          bulk_commit();
         }
       }
       // every TMEM read of O is complete: item n + 1's first PV may overwrite it
@@ -1344,17 +1347,17 @@ cudaError_t kvc_launch_attn_tc(kvc_cache* c, const void* q, void* out, int n_q, 
     if (items > INT32_MAX) return cudaErrorInvalidValue;
     dim3 grid((unsigned)(items < c->num_sms ? items : c->num_sms));
     if (cfg.dtype == KVC_BF16)
-      k_attn_tc<true><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
-    else
-      k_attn_tc<false><<<grid, kThreads, smem_bytes(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
-    return cudaGetLastError();
+      return kvc_launch_pdl(k_attn_tc<true>, grid, dim3(kThreads), smem_bytes(), s, tm_q, c->tm_k, c->tm_v, tm_o,
+                            c->meta, p);
+    return kvc_launch_pdl(k_attn_tc<false>, grid, dim3(kThreads), smem_bytes(), s, tm_q, c->tm_k, c->tm_v, tm_o,
+                          c->meta, p);
   }
   const int64_t items = (int64_t)((n_q + kBM - 1) / kBM) * cfg.heads * cfg.batch;
   if (items > INT32_MAX) return cudaErrorInvalidValue;
   dim3 grid((unsigned)(items < c->num_sms ? items : c->num_sms));    // persistent: one CTA per SM
   if (cfg.dtype == KVC_BF16)
-    k_attn_1q<true><<<grid, kThreads1, smem_bytes1(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
-  else
-    k_attn_1q<false><<<grid, kThreads1, smem_bytes1(), s>>>(tm_q, c->tm_k, c->tm_v, tm_o, c->meta, p);
-  return cudaGetLastError();
+    return kvc_launch_pdl(k_attn_1q<true>, grid, dim3(kThreads1), smem_bytes1(), s, tm_q, c->tm_k, c->tm_v, tm_o,
+                          c->meta, p);
+  return kvc_launch_pdl(k_attn_1q<false>, grid, dim3(kThreads1), smem_bytes1(), s, tm_q, c->tm_k, c->tm_v, tm_o,
+                        c->meta, p);
 }
