@@ -26,8 +26,8 @@
 // The append instantiation is a whole decode step in one launch: each row's prefix is
 // its filled count, the new token's key and value come from the caller's buffers and
 // join the final merge in fp32 (score and weight), block 0 of each (row, kv head)
-// stores them at the row's next slot, and the last block to arrive on a counter in the
-// meta block advances every row's counters.
+// stores them at the row's next slot once it has streamed its tiles, and the last block
+// to arrive on a counter in the meta block advances every row's counters.
 #include "kvc_internal.h"
 
 #include <cuda_bf16.h>
@@ -299,8 +299,9 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
     if (warp == 0) {
       // Warp 0 alone (the producer warp goes on to issue the first loads, whose latency
       // covers this): arrive, advance every row if this block is the last to arrive, and
-      // (block 0 of the pair) store the new token's K and V rows of this kv head at slot
-      // `len`, which no block of this launch reads (its key comes from k_new / v_new).
+      // load the new token's key and value (block 0 of the pair stores them at slot `len`
+      // after its stream: no block of this launch reads that slot, and a store there
+      // while the first tiles load made the step slower).
       constexpr unsigned kAll = 0xffffffffu;
       int upd = 0;
       if (lane == 0) {
@@ -335,16 +336,6 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
           nv[i] = v_new[kv_off + lane + 32 * i];
 #pragma unroll
           for (int gg = 0; gg < G; ++gg) nq[gg][i] = q[((int64_t)b * g.H + kvh * G + gg) * D + lane + 32 * i];
-        }
-      }
-      constexpr int kRowVecs = D * (int)sizeof(T) / 16;
-      if (row_ok && split == 0) {
-        for (int i = lane; i < 2 * kRowVecs; i += 32) {
-          const int t = i / kRowVecs, c = i - t * kRowVecs;
-          const uint4* src = reinterpret_cast<const uint4*>((t ? v_new : k_new) + ((int64_t)b * g.Hkv + kvh) * D) + c;
-          uint4* dst =
-              reinterpret_cast<uint4*>((t ? v_store : k_store) + (((int64_t)b * g.cap + len) * g.Hkv + kvh) * D) + c;
-          *dst = __ldg(src);
         }
       }
     }
@@ -553,6 +544,15 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   }
   __syncthreads();
   if (threadIdx.x == 0 && s_wc.abort) atomicOr(meta + KVC_META_ERR, KVC_DEV_TIMEOUT);
+  if (app && split == 0 && warp == 0) {   // the new token's K and V rows, at slot len
+    T* kd = k_store + (((int64_t)b * g.cap + len) * g.Hkv + kvh) * D;
+    T* vd = v_store + (((int64_t)b * g.cap + len) * g.Hkv + kvh) * D;
+#pragma unroll
+    for (int i = 0; i < kNew; ++i) {
+      kd[lane + 32 * i] = nk[i];
+      vd[lane + 32 * i] = nv[i];
+    }
+  }
 
   // ---- this block's partial: merge the warps ---------------------------------
   if (solo) {   // the whole row: normalise and write the output
