@@ -19,7 +19,7 @@
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kMergeUnroll = 4;
+constexpr int kMergeUnroll = 2;
 
 __device__ __forceinline__ float ld(const float* p) { return *p; }
 __device__ __forceinline__ float ld(const __half* p) { return __half2float(*p); }
