@@ -223,7 +223,7 @@ k_decode(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUten
   float (*s_acc)[G][D] = reinterpret_cast<float (*)[G][D]>(dsm);
   __shared__ float s_ml[kWarps][G][2];
   __shared__ float s_inv[G], s_max[G];
-  __shared__ int s_last, s_upd;
+  __shared__ int s_last;
   __shared__ float s_snew[G], s_pnew[G];   // append: the new key's score (exp2 domain) and weight
   __shared__ float s_vnew[D];               // append: the new token's value row
   __shared__ WaitCtl s_wc;
